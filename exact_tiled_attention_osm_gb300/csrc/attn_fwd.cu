@@ -1,0 +1,509 @@
+// attn_fwd.cu — exact softmax attention forward on sm_103a tensor cores.
+//
+// The method: "Online softmax" (zerotofrontier.app), section "Blocks, the
+// bridge to FlashAttention": hold a block of query rows, stream key/value
+// blocks past it, form the block of scores with a matrix product, summarise it
+// per row and merge that summary into the running one (running max m, running
+// sum l, unnormalised output O~), rescaling the old state by 2^(m_old - m_new)
+// when the max grows; divide once at the end and keep lse = m + log l
+// (section "From weights to outputs").  Masks are applied inside the tile loop
+// ("Online softmax", guide.dupenodi.dev, "Walking through it"); fully masked
+// rows get the merge identity's finalisation (output 0, lse -inf).  Base-2
+// exponentials with log2(e) folded into the scale ("Precision, and what can
+// still go wrong").
+//
+// GB300 mapping (one CTA per SM, persistent over work items):
+//   work item  = (b, h, pair of 128-row query tiles); both tiles share every
+//                streamed K/V tile, and alternate on the tensor core so one
+//                tile's softmax overlaps the other tile's matrix products.
+//   warp 0     TMA producer: Q tiles once per item, K_j / V_j through a ring
+//              of shared-memory slots (128-byte swizzle).
+//   warp 1     MMA issuer (one thread): S_t = Q_t K_j^T into TMEM, then
+//              O~_t += P_t V_j with P_t read straight from TMEM.
+//   warps 4-7  softmax for query tile 0; warps 8-11 for tile 1.  One thread
+//              per query row: TMEM -> registers, mask, row max, exp2, row sum,
+//              P as bf16 back into TMEM over S, rescale O~ in TMEM when the
+//              max has grown, and the final O = O~ / l, lse epilogue.
+//   TMEM       512 columns: S_0 | S_1 | O~_0 | O~_1 (128 fp32 columns each).
+// The rescale is taken only when the new max exceeds the reference by more
+// than kTau (base-2 units); every identity of the recurrence holds for any
+// common reference ("Precision, and what can still go wrong", second point),
+// so skipping a small rescale changes no result, it only lets P reach 2^kTau.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tmap.h"
+
+namespace osm {
+namespace attn {
+
+using namespace ptx;
+
+constexpr int kHeadDim = 128;
+constexpr int kRows = 128;   // query rows per tile (MMA M)
+constexpr int kKeys = 128;   // keys per K/V tile (MMA N of QK^T, K of PV)
+constexpr int kSlots = 4;    // K/V ring slots, one 32 KB tile each
+constexpr uint32_t kTileBytes = kRows * kHeadDim * 2;  // 32768
+constexpr uint32_t kBoxBytes = 128 * 64 * 2;           // one TMA box: 64 columns x 128 rows
+constexpr int kThreads = 384;
+constexpr float kTau = 8.0f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kNegInf = -__builtin_huge_valf();
+
+// shared memory map (offsets from a 1024-byte aligned base)
+constexpr uint32_t kSmemQ = 0;
+constexpr uint32_t kSmemKV = 2 * kTileBytes;
+constexpr uint32_t kSmemBar = kSmemKV + kSlots * kTileBytes;
+enum Bar : uint32_t {
+  Q_FULL = 0,       // [2]
+  Q_EMPTY = 2,
+  KV_FULL = 3,      // [kSlots]
+  KV_EMPTY = 3 + kSlots,
+  S_FULL = 3 + 2 * kSlots,   // [2]
+  P_FULL = S_FULL + 2,       // [2]
+  O_FULL = P_FULL + 2,       // [2]
+  O_EMPTY = O_FULL + 2,      // [2]
+  DRAIN = O_EMPTY + 2,
+  NUM_BARS
+};
+constexpr uint32_t kSmemTmemSlot = kSmemBar + 8 * NUM_BARS;
+constexpr uint32_t kSmemAbort = kSmemTmemSlot + 4;
+constexpr uint32_t kSmemBytes = kSmemAbort + 4 + 1024;  // + alignment slack
+
+// TMEM columns
+constexpr uint32_t kTmemS = 0;
+constexpr uint32_t kTmemO = 256;
+
+constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);  // Q, K both K-major
+constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, true);  // V is MN-major
+
+// error-word sites (kernel id 1 in the top byte)
+constexpr unsigned kSite = 0x01000000u;
+
+struct Params {
+  int B, H, Nq, Nk;
+  int causal;
+  int npairs;
+  int num_items;
+  float scale_log2;
+  const int32_t* key_len;
+  __nv_bfloat16* o;
+  float* lse;
+  unsigned int* err;
+};
+
+struct Item {
+  int bh, q0, n_kv, kv_len;
+};
+
+__device__ __forceinline__ Item item_info(const Params& p, int item) {
+  Item it;
+  const int within = item % p.npairs;
+  it.bh = item / p.npairs;
+  const int pair = p.causal ? (p.npairs - 1 - within) : within;  // causal: longest first
+  it.q0 = pair * 2 * kRows;
+  const int b = it.bh / p.H;
+  int L = p.key_len ? p.key_len[b] : p.Nk;
+  L = L < 0 ? 0 : (L > p.Nk ? p.Nk : L);
+  it.kv_len = L;
+  int end = L;
+  if (p.causal) {
+    const int last_row = min(it.q0 + 2 * kRows - 1, p.Nq - 1);
+    end = min(L, max(0, last_row + 1 + (p.Nk - p.Nq)));
+  }
+  it.n_kv = (end + kKeys - 1) / kKeys;
+  return it;
+}
+
+__device__ unsigned int g_err_word;
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sQ = sbase + kSmemQ, sKV = sbase + kSmemKV;
+  auto bar = [&](uint32_t i) { return sbase + kSmemBar + 8 * i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSmemTmemSlot);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(Q_FULL + t), 1);
+      mbar_init(bar(S_FULL + t), 1);
+      mbar_init(bar(P_FULL + t), 4);
+      mbar_init(bar(O_FULL + t), 1);
+      mbar_init(bar(O_EMPTY + t), 4);
+    }
+    mbar_init(bar(Q_EMPTY), 1);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(bar(KV_FULL + s), 1);
+      mbar_init(bar(KV_EMPTY + s), 1);
+    }
+    mbar_init(bar(DRAIN), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ TMA producer
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    uint32_t slot = 0, ph = 0, qe_ph = 0;
+    uint32_t fill_mask = 0, fill_ph = 0;  // slots ever filled / parity of their last fill
+    int q_fill = -1;
+    int loaded = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x) {
+      const Item it = item_info(p, item);
+      if (it.n_kv == 0) continue;
+      if (loaded > 0) {
+        if (!(ok = wait_bounded(bar(Q_EMPTY), qe_ph, abort_flag, p.err, kSite | 1))) break;
+        qe_ph ^= 1;
+      }
+      for (int t = 0; t < 2; ++t) {
+        mbar_arrive_expect_tx(bar(Q_FULL + t), kTileBytes);
+        for (int c = 0; c < 2; ++c)
+          tma_load_3d(sQ + t * kTileBytes + c * kBoxBytes, &tm_q, bar(Q_FULL + t), c * 64,
+                      it.q0 + t * kRows, it.bh);
+      }
+      q_fill = loaded & 1;
+      ++loaded;
+      for (int j = 0; ok && j < it.n_kv; ++j) {
+        for (int kv = 0; kv < 2; ++kv) {
+          if (!(ok = wait_bounded(bar(KV_EMPTY + slot), ph ^ 1, abort_flag, p.err, kSite | 2)))
+            break;
+          mbar_arrive_expect_tx(bar(KV_FULL + slot), kTileBytes);
+          const CUtensorMap* tm = kv ? &tm_v : &tm_k;
+          for (int c = 0; c < 2; ++c)
+            tma_load_3d(sKV + slot * kTileBytes + c * kBoxBytes, tm, bar(KV_FULL + slot), c * 64,
+                        j * kKeys, it.bh);
+          fill_mask |= 1u << slot;
+          fill_ph = (fill_ph & ~(1u << slot)) | (ph << slot);
+          if (++slot == kSlots) {
+            slot = 0;
+            ph ^= 1;
+          }
+        }
+      }
+    }
+    if (!ok) {  // let every copy this thread started land before the CTA exits
+      for (int s = 0; s < kSlots; ++s)
+        if (fill_mask >> s & 1u) wait_drain(bar(KV_FULL + s), fill_ph >> s & 1u, 200000000ull);
+      if (q_fill >= 0)
+        for (int t = 0; t < 2; ++t) wait_drain(bar(Q_FULL + t), q_fill, 200000000ull);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    uint32_t slot = 0, ph = 0, qf_ph = 0;
+    uint32_t pf_ph[2] = {0, 0}, oe_ph[2] = {0, 0};
+    int done = 0;
+    bool ok = true;
+    const uint64_t dK = sdesc_sw128(0, 16, 1024);       // K-major template (address added)
+    const uint64_t dV = sdesc_sw128(0, 16384, 1024);    // MN-major template
+    for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x) {
+      const Item it = item_info(p, item);
+      if (it.n_kv == 0) continue;
+      if (!(ok = wait_bounded(bar(Q_FULL), qf_ph, abort_flag, p.err, kSite | 3))) break;
+      if (!(ok = wait_bounded(bar(Q_FULL + 1), qf_ph, abort_flag, p.err, kSite | 3))) break;
+      qf_ph ^= 1;
+      tc_fence_after();
+      bool first_pv[2] = {true, true};
+      uint32_t v_slot = 0, v_ph = 0;
+      // P_t V_{j-1} for tile t (waits for the softmax of tile t)
+      auto issue_pv = [&](int t) -> bool {
+        if (!wait_bounded(bar(P_FULL + t), pf_ph[t], abort_flag, p.err, kSite | 5)) return false;
+        pf_ph[t] ^= 1;
+        if (first_pv[t] && done > 0) {
+          if (!wait_bounded(bar(O_EMPTY + t), oe_ph[t], abort_flag, p.err, kSite | 6))
+            return false;
+          oe_ph[t] ^= 1;
+        }
+        tc_fence_after();
+        const uint32_t vaddr = sKV + v_slot * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          mma_ts(tbase + kTmemO + t * 128, tbase + kTmemS + t * 128 + kk * 8,
+                 dV + ((vaddr + kk * 2048) >> 4), kIdescPV, (!first_pv[t] || kk > 0) ? 1u : 0u);
+        }
+        first_pv[t] = false;
+        return true;
+      };
+      for (int j = 0; ok && j < it.n_kv; ++j) {
+        const uint32_t k_slot = slot;
+        if (!(ok = wait_bounded(bar(KV_FULL + k_slot), ph, abort_flag, p.err, kSite | 4))) break;
+        if (++slot == kSlots) { slot = 0; ph ^= 1; }
+        const uint32_t nv_slot = slot, nv_ph = ph;
+        if (++slot == kSlots) { slot = 0; ph ^= 1; }
+        if (j > 0) {
+          if (!(ok = wait_bounded(bar(KV_FULL + v_slot), v_ph, abort_flag, p.err, kSite | 4)))
+            break;
+        }
+        tc_fence_after();
+        const uint32_t kaddr = sKV + k_slot * kTileBytes;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j > 0 && !(ok = issue_pv(t))) break;
+          const uint32_t qaddr = sQ + t * kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+            mma_ss(tbase + kTmemS + t * 128, dK + ((qaddr + off) >> 4), dK + ((kaddr + off) >> 4),
+                   kIdescS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(S_FULL + t));
+        }
+        if (!ok) break;
+        mma_commit(bar(KV_EMPTY + k_slot));
+        if (j > 0) mma_commit(bar(KV_EMPTY + v_slot));
+        if (j == it.n_kv - 1) mma_commit(bar(Q_EMPTY));
+        v_slot = nv_slot;
+        v_ph = nv_ph;
+      }
+      if (!ok) break;
+      if (!(ok = wait_bounded(bar(KV_FULL + v_slot), v_ph, abort_flag, p.err, kSite | 4))) break;
+      for (int t = 0; t < 2 && ok; ++t) {
+        if (!(ok = issue_pv(t))) break;
+        mma_commit(bar(O_FULL + t));
+      }
+      if (!ok) break;
+      mma_commit(bar(KV_EMPTY + v_slot));
+      ++done;
+    }
+    if (!ok) {  // wait for every MMA already issued before TMEM is released
+      mma_commit(bar(DRAIN));
+      wait_drain(bar(DRAIN), 0, 200000000ull);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int t = (warp - 4) >> 2;                  // query tile of this warpgroup
+    const int wq = warp & 3;                        // TMEM lane quarter
+    const uint32_t lane_off = static_cast<uint32_t>(32 * wq) << 16;
+    const uint32_t tS = tbase + lane_off + kTmemS + t * 128;
+    const uint32_t tO = tbase + lane_off + kTmemO + t * 128;
+    const float sl2 = p.scale_log2;
+    uint32_t sf_ph = 0, of_ph = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x) {
+      const Item it = item_info(p, item);
+      const int row = it.q0 + t * kRows + 32 * wq + lane;
+      const bool row_ok = row < p.Nq;
+      const int64_t orow = static_cast<int64_t>(it.bh) * p.Nq + row;
+      if (it.n_kv == 0) {
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(p.o + orow * kHeadDim);
+#pragma unroll
+          for (int i = 0; i < kHeadDim / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+          p.lse[orow] = kNegInf;
+        }
+        continue;
+      }
+      int limit = it.kv_len;
+      if (p.causal) limit = min(limit, row + 1 + (p.Nk - p.Nq));
+      float m_ref = kNegInf, l = 0.f;
+      for (int j = 0; j < it.n_kv; ++j) {
+        ok = __all_sync(0xffffffffu,
+                        wait_bounded(bar(S_FULL + t), sf_ph, abort_flag, p.err, kSite | 7));
+        if (!ok) break;
+        sf_ph ^= 1;
+        tc_fence_after();
+        uint32_t sr[128];
+        tmem_ld_x128(tS, sr);
+        const int k0 = j * kKeys;
+        if (__any_sync(0xffffffffu, k0 + kKeys > limit)) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (k0 + c >= limit) sr[c] = __float_as_uint(kNegInf);
+        }
+        float mx[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
+#pragma unroll
+        for (int c = 0; c < 128; c += 4) {
+          mx[0] = fmaxf(mx[0], __uint_as_float(sr[c]));
+          mx[1] = fmaxf(mx[1], __uint_as_float(sr[c + 1]));
+          mx[2] = fmaxf(mx[2], __uint_as_float(sr[c + 2]));
+          mx[3] = fmaxf(mx[3], __uint_as_float(sr[c + 3]));
+        }
+        const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+        const float m_new = fmaxf(m_ref, m_tile);
+        float alpha = 1.f;
+        bool resc = false;
+        if (m_ref == kNegInf) {
+          m_ref = m_new;  // nothing summed yet: l = 0 and O~ = 0
+        } else if (m_new > m_ref + kTau) {
+          alpha = ex2(m_ref - m_new);
+          l *= alpha;
+          m_ref = m_new;
+          resc = true;
+        }
+        if (__any_sync(0xffffffffu, resc)) {
+          // O~ has every earlier P V product in it (the commit that signalled S
+          // also covers the previous P V), and nothing writes it until P is ready
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t orr[32];
+            tmem_ld_x32(tO + 32 * c, orr);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+            tmem_st_x32(tO + 32 * c, orr);
+          }
+        }
+        const float nref = (m_ref == kNegInf) ? 0.f : -m_ref;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), sl2, nref));
+          const float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, nref));
+          ls[c & 3] += p0 + p1;
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+          pk[c] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        tmem_st_x64(tS, pk);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(P_FULL + t));
+      }
+      if (!ok) break;
+      // epilogue: O = O~ / l, lse = ln2 * (m + log2 l)
+      ok = __all_sync(0xffffffffu,
+                      wait_bounded(bar(O_FULL + t), of_ph, abort_flag, p.err, kSite | 8));
+      if (!ok) break;
+      of_ph ^= 1;
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t orr[32];
+        tmem_ld_x32(tO + 32 * c, orr);
+        if (row_ok) {
+          uint32_t pk2[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(orr[2 * e]) * inv,
+                                                      __uint_as_float(orr[2 * e + 1]) * inv);
+            pk2[e] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(p.o + orow * kHeadDim + 32 * c);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dst[e] = make_uint4(pk2[4 * e], pk2[4 * e + 1], pk2[4 * e + 2], pk2[4 * e + 3]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(O_EMPTY + t));
+      if (row_ok) p.lse[orow] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : kNegInf;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tbase, 512);
+}
+
+// every query row fully masked (no key at all): O = 0, lse = -inf
+__global__ void attn_empty_kernel(__nv_bfloat16* o, float* lse, int64_t rows) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < rows * (kHeadDim / 8)) reinterpret_cast<uint4*>(o)[i] = make_uint4(0, 0, 0, 0);
+  if (i < rows) lse[i] = kNegInf;
+}
+
+}  // namespace attn
+
+int sm_count_current_device() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
+  return n > 0 ? n : 1;
+}
+
+cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                            const int32_t* key_len, cudaStream_t s, bool* tmap_ok) {
+  using namespace attn;
+  *tmap_ok = true;
+  (void)d;
+  const int64_t rows = static_cast<int64_t>(B) * H * Nq;
+  if (Nk == 0) {
+    const int64_t n = rows * (kHeadDim / 8);
+    attn_empty_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(
+        static_cast<__nv_bfloat16*>(o), lse, rows);
+    return cudaGetLastError();
+  }
+  CUtensorMap tq, tk, tv;
+  const uint64_t BH = static_cast<uint64_t>(B) * H;
+  if (!make_tmap_bf16_3d(&tq, q, kHeadDim, Nq, BH, 64, kRows) ||
+      !make_tmap_bf16_3d(&tk, k, kHeadDim, Nk, BH, 64, kKeys) ||
+      !make_tmap_bf16_3d(&tv, v, kHeadDim, Nk, BH, 64, kKeys)) {
+    *tmap_ok = false;
+    return cudaSuccess;
+  }
+  Params p;
+  p.B = B;
+  p.H = H;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.causal = causal ? 1 : 0;
+  p.npairs = (Nq + 2 * kRows - 1) / (2 * kRows);
+  const int64_t items = static_cast<int64_t>(BH) * p.npairs;
+  p.num_items = static_cast<int>(items);
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.key_len = key_len;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  void* errp = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&errp, g_err_word);
+  if (e != cudaSuccess) return e;
+  p.err = static_cast<unsigned int*>(errp);
+  // the shared-memory opt-in is per function and per device
+  static unsigned long long attr_done = 0;
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(attr_done & bit)) {
+    e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_done |= bit;
+  }
+  const int grid = static_cast<int>(items < sm_count_current_device() ? items
+                                                                      : sm_count_current_device());
+  attn_fwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_device_error(cudaStream_t s, uint32_t* word) {
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return e;
+  unsigned int w = 0;
+  e = cudaMemcpyFromSymbol(&w, attn::g_err_word, sizeof(w));
+  if (e != cudaSuccess) return e;
+  if (w != 0) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(attn::g_err_word, &zero, sizeof(zero));
+    if (e != cudaSuccess) return e;
+  }
+  *word = w;
+  return cudaSuccess;
+}
+
+}  // namespace osm

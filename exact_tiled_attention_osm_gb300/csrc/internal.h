@@ -1,0 +1,31 @@
+// internal.h — launchers shared between the C-ABI front end (api.cu) and the
+// kernel translation units.  Arguments are already validated by the caller.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "osm.h"
+
+namespace osm {
+
+int sm_count_current_device();
+
+// softmax_rows.cu
+cudaError_t launch_softmax_rows(const float* x, float* y, int64_t rows, int64_t cols,
+                                cudaStream_t s);
+
+// attn_fwd.cu
+cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                            const int32_t* key_len, cudaStream_t s, bool* tmap_ok);
+cudaError_t read_and_clear_device_error(cudaStream_t s, uint32_t* word);
+
+// decode.cu
+size_t decode_workspace_bytes(int B, int H, int d, int S);
+cudaError_t launch_decode_splitkv(osm_dtype dt, const void* q, const void* k, const void* v,
+                                  void* o, float* lse, int B, int H, int Nk, int d, float scale,
+                                  const int32_t* key_len, int S, void* ws, cudaStream_t s);
+cudaError_t launch_lse_merge(const float* o_parts, const float* lse_parts, int S, int64_t rows,
+                             int d, osm_dtype out_dt, void* o, float* lse, cudaStream_t s);
+
+}  // namespace osm

@@ -1,0 +1,181 @@
+/*
+ * osm.h — C ABI of libosm: exact softmax attention by the online-softmax
+ * recurrence, for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * The operations follow three web pages on one subject:
+ *   [P1] "Online Softmax: How FlashAttention Skips the N×N Matrix" (dev.to)
+ *   [P2] "Online softmax" (guide.dupenodi.dev)
+ *   [P3] "Online softmax" (zerotofrontier.app, chapter 12.2)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument is DEVICE memory owned by the caller.  The library
+ *    never allocates, frees or synchronises; it only launches kernels.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream).  Outputs are ready when the stream reaches that point.
+ *  - Tensors are dense and contiguous, row-major, innermost dimension last.
+ *  - Arguments are validated on the host before anything is launched; a bad
+ *    argument returns OSM_ERR_INVALID_VALUE (or OSM_ERR_UNSUPPORTED for a valid
+ *    but unimplemented case) and launches nothing.  A failed launch returns
+ *    OSM_ERR_CUDA.  No call aborts the process or throws.
+ *  - Scores are s = scale * (q . k).  Log-sum-exp outputs are natural-log
+ *    values of the scaled scores.  Kernels work in base 2 internally (log2(e)
+ *    is folded into the scale once) and convert back ([P3] "Precision").
+ *  - A query row with no visible key (a fully masked row) gets output 0 and
+ *    log-sum-exp -inf ([P3] "Precision": such a row ends with l = 0 and is
+ *    handled explicitly; its summary is the merge identity (-inf, 0, 0)).
+ *  - Device-side waits are bounded.  If one runs out, the kernel records an
+ *    error word, drains its own copies and returns; osm_device_status()
+ *    reports it.  Outputs of that launch are then undefined.
+ */
+#ifndef OSM_H_
+#define OSM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *osm_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  OSM_OK = 0,
+  OSM_ERR_INVALID_VALUE = 1, /* null pointer, bad size, misalignment, small workspace */
+  OSM_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement (e.g. d) */
+  OSM_ERR_CUDA = 3,          /* a CUDA launch or runtime call failed */
+  OSM_ERR_TIMEOUT = 4        /* a bounded device-side wait ran out (osm_device_status) */
+} osm_status;
+
+typedef enum { OSM_F32 = 0, OSM_BF16 = 1 } osm_dtype;
+
+/*
+ * osm_softmax_rows — softmax of every row of an fp32 matrix.
+ *
+ * Defines: y[r, i] = exp(x[r, i] - m_r) / l_r with m_r the row maximum and
+ * l_r = sum_i exp(x[r, i] - m_r)  ([P3] "Three passes, and why that is a
+ * problem").  Computed with the online normaliser ([P3] "The recurrence, and
+ * a proof that it is right"): per-thread (m, l) summaries merged exactly
+ * ([P3] "Merging partial results"), then one scaling pass.  Each element is
+ * read from HBM once and written once.
+ *
+ *   x     [rows, cols] fp32, device, read only.
+ *   y     [rows, cols] fp32, device; may equal x (in place); must not
+ *         otherwise overlap x.
+ *   rows, cols >= 0 (rows * cols == 0 is a no-op returning OSM_OK).
+ * Entries must be finite or -inf.  An all -inf row gives zeros.
+ * Fast path: x, y 16-byte aligned, cols % 4 == 0, cols <= 131072; any other
+ * shape runs a generic two-pass kernel (x read twice, y written once).
+ */
+osm_status osm_softmax_rows(const float *x, float *y, int64_t rows, int64_t cols,
+                            osm_stream_t stream);
+
+/*
+ * osm_attn_fwd — exact softmax attention forward, BF16 in, FP32 state.
+ *
+ * Defines: for every (b, h) and query row i,
+ *   s_ij = scale * (q_i . k_j),  masked to -inf where j >= key_len[b] or
+ *          (causal and j > i + (Nk - Nq))   (causal is bottom-right aligned),
+ *   o_i = softmax(s_i) V,   lse_i = log sum_j exp(s_ij).
+ * Computed tile by tile ([P3] "Blocks, the bridge to FlashAttention"): 128
+ * query rows against streamed 128-key tiles, running max m, running sum l and
+ * unnormalised output O~ in FP32, rescaled by 2^(m_old - m_new) when the max
+ * grows, masks applied inside the tile loop ([P2] "Walking through it"), one
+ * division at the end, lse = m + log l ([P3] "From weights to outputs").
+ * No score matrix is written to memory.
+ *
+ *   q     [B, H, Nq, d] bf16;  k, v [B, H, Nk, d] bf16 (read only).
+ *   o     [B, H, Nq, d] bf16 (written);  lse [B, H, Nq] fp32 (written).
+ *   d     must be 128 (other values return OSM_ERR_UNSUPPORTED).
+ *   scale finite and > 0 (e.g. 1/sqrt(d)).
+ *   causal 0 or 1.
+ *   key_len device int32[B] (valid keys per batch entry, clamped to [0, Nk]
+ *         on the device) or NULL for "all Nk keys valid".
+ *   B, H, Nq >= 0 (a zero makes the call a no-op), Nk >= 0.
+ *   q, k, v, o must be 16-byte aligned; lse 4-byte aligned.
+ * Keys past key_len are never allowed into the running sums; their K/V
+ * contents must be finite (a NaN/Inf there would poison the tensor-core dot
+ * products of the same tile) but otherwise do not affect the result.
+ */
+osm_status osm_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                        int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                        const int32_t *key_len, osm_stream_t stream);
+
+/*
+ * osm_attn_decode_splitkv_workspace_bytes — bytes of device workspace that
+ * osm_attn_decode_splitkv needs for these sizes (0 if a size is invalid).
+ *
+ * Workspace layout (fp32, R = B*H rows, S = num_splits), each section starting
+ * on a 256-byte boundary:
+ *   m  [S][R]      running max of split s for row r (natural-log units)
+ *   l  [S][R]      sum over the split of exp(s_j - m)
+ *   o~ [S][R][d]   sum over the split of exp(s_j - m) v_j
+ * Section offsets: m at 0, l at A, o~ at 2A with A = round_up(4*S*R, 256).
+ * An empty split holds the merge identity (-inf, 0, 0).
+ */
+size_t osm_attn_decode_splitkv_workspace_bytes(int B, int H, int d, int num_splits);
+
+/*
+ * osm_attn_decode_splitkv — one query per (b, h) against a long KV cache,
+ * with the keys split into num_splits pieces processed by separate thread
+ * blocks, each piece summarised as (m, l, o~), then merged exactly
+ * ([P3] "Merging partial results" and "The same merge, in log-sum-exp form":
+ * Flash-Decoding splits one query's keys across thread blocks and merges).
+ *
+ *   dt    OSM_BF16 (q, k, v, o in bf16) or OSM_F32 (all fp32).
+ *   q     [B, H, 1, d];  k, v [B, H, Nk, d];  o [B, H, 1, d] in dt.
+ *   lse   [B, H] fp32.
+ *   d     64 or 128.
+ *   key_len device int32[B] (clamped to [0, Nk]) or NULL (= Nk).
+ *   num_splits 1..256.  Split s of batch entry b covers keys
+ *         [s*c, min((s+1)*c, L_b)) with c = ceil(L_b / num_splits), so the
+ *         valid length, not Nk, is divided; keys past L_b are never read.
+ *   workspace >= osm_attn_decode_splitkv_workspace_bytes(B, H, d, num_splits)
+ *         bytes of device memory, 256-byte aligned, owned by the caller; it
+ *         holds the per-split summaries (layout above) after the call.
+ *   q, k, v, o 16-byte aligned.
+ * Two launches on `stream`: the split kernel, then the merge kernel.
+ */
+osm_status osm_attn_decode_splitkv(osm_dtype dt, const void *q, const void *k, const void *v,
+                                   void *o, float *lse, int B, int H, int Nk, int d,
+                                   float scale, const int32_t *key_len, int num_splits,
+                                   void *workspace, size_t workspace_bytes,
+                                   osm_stream_t stream);
+
+/*
+ * osm_lse_merge — merge S normalised partial results per row in
+ * log-sum-exp form ([P3] "The same merge, in log-sum-exp form"):
+ *   lse = log sum_s exp(lse_s),   o = sum_s exp(lse_s - lse) o_s.
+ * A part with lse_s = -inf has weight 0; a row whose parts are all -inf gets
+ * o = 0, lse = -inf.  Parts are merged in the fixed order s = 0 .. S-1.
+ *
+ *   o_parts   [S][rows][d] fp32, 16-byte aligned.
+ *   lse_parts [S][rows] fp32.
+ *   S 1..1024;  rows >= 0;  d 64 or 128.
+ *   out_dt    dtype of o: OSM_F32 or OSM_BF16.
+ *   o [rows][d] (out_dt), lse [rows] fp32.
+ */
+osm_status osm_lse_merge(const float *o_parts, const float *lse_parts, int S, int64_t rows,
+                         int d, osm_dtype out_dt, void *o, float *lse, osm_stream_t stream);
+
+/* Text for a status code (static storage; never NULL). */
+const char *osm_status_string(osm_status status);
+
+/*
+ * osm_device_status — synchronise `stream`, then read and clear the current
+ * device's error word that bounded waits write.  *word = 0 means no device
+ * wait ran out since the last call; otherwise it identifies the wait site and
+ * the return value is OSM_ERR_TIMEOUT.  Returns OSM_ERR_CUDA if the
+ * synchronisation itself fails.  Not a hot-path call.
+ */
+osm_status osm_device_status(osm_stream_t stream, uint32_t *word);
+
+/* ABI version of this header (major * 100 + minor). */
+int osm_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OSM_H_ */

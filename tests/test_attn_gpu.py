@@ -1,0 +1,157 @@
+"""Attention forward on the GPU against the float64 oracle.
+
+Bar (BF16 inputs, float64 oracle on the same bf16-rounded inputs):
+  O:   |O_gpu - O_ref| <= 1e-2 + 2^-8 |O_ref|   — 1e-2 on the value, plus the
+       output's own bf16 storage rounding (at most half a bf16 ulp <= 2^-8 |O|);
+  LSE: |lse_gpu - lse_ref| <= 1e-3, and -inf exactly where the oracle has -inf;
+  masked keys contribute exactly zero (bitwise test across two paddings).
+"""
+import numpy as np
+import pytest
+import torch
+
+import exact_tiled_attention_osm_gb300 as osm
+import oracle
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+O_TOL, O_REL, LSE_TOL = 1e-2, 2.0 ** -8, 1e-3
+
+
+def check(o, lse, ro, rl):
+    o, lse = W.as_f64(o), W.as_f64(lse)
+    assert np.array_equal(np.isneginf(lse), np.isneginf(rl)), "masked-row pattern differs"
+    fin = np.isfinite(rl)
+    err_o = np.abs(o - ro)
+    assert np.all(np.isfinite(o))
+    assert float(np.max(err_o - O_REL * np.abs(ro))) <= O_TOL, f"O err {err_o.max()}"
+    if fin.any():
+        assert float(np.max(np.abs(lse[fin] - rl[fin]))) <= LSE_TOL
+    return float(err_o.max())
+
+
+def run(case, dev="cuda"):
+    kl = case.key_len.to(dev) if case.key_len is not None else None
+    o, lse = osm.attn_fwd(case.q.to(dev), case.k.to(dev), case.v.to(dev), case.scale, case.causal,
+                          kl)
+    assert osm.device_status() == 0
+    return o, lse
+
+
+def oracle_of(case, rows=None, bh=None):
+    q, k, v = case.q, case.k, case.v
+    kl = case.key_len.numpy() if case.key_len is not None else None
+    if bh is not None:  # restrict to a list of (b, h)
+        outs = [oracle.attention_ref(W.as_f64(q[b:b + 1, h:h + 1]), W.as_f64(k[b:b + 1, h:h + 1]),
+                                     W.as_f64(v[b:b + 1, h:h + 1]), case.scale, case.causal,
+                                     None if kl is None else kl[b:b + 1], rows=rows)
+                for b, h in bh]
+        return outs
+    return oracle.attention_ref(W.as_f64(q), W.as_f64(k), W.as_f64(v), case.scale, case.causal,
+                                kl, rows=rows)
+
+
+SHAPES = [(1, 1, 1, 1), (1, 1, 63, 63), (1, 2, 64, 64), (1, 1, 65, 65), (2, 1, 127, 129),
+          (1, 1, 129, 127), (1, 2, 300, 300), (1, 1, 256, 256), (1, 1, 257, 1000),
+          (1, 1, 1000, 257), (2, 2, 513, 513), (1, 1, 1, 4097), (1, 1, 4097, 4097)]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", SHAPES)
+def test_shapes(cuda_ok, shape, causal):
+    B, H, Nq, Nk = shape
+    case = W.attention(sum(shape) + 100 * causal, B, H, Nq, Nk, 128, causal, (max(1, Nk // 3), Nk))
+    o, lse = run(case)
+    check(o, lse, *oracle_of(case))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_len_edges(cuda_ok, causal):
+    N = 300
+    case = W.attention(21, 4, 2, N, N, 128, causal, None)
+    case.key_len = torch.tensor([0, 1, N - 1, N], dtype=torch.int32)
+    o, lse = run(case)
+    ro, rl = oracle_of(case)
+    check(o, lse, ro, rl)
+    assert torch.all(o[0] == 0) and torch.all(torch.isneginf(lse[0]))
+    # one visible key: O = v_0 exactly (weight 1, bf16 value reproduced exactly)
+    v0 = case.v[1, :, 0:1, :].to(o.device).expand(-1, N, -1)
+    assert torch.equal(o[1], v0)
+
+
+def test_no_keys_and_more_queries_than_keys(cuda_ok):
+    case = W.attention(22, 1, 2, 100, 0, 128, False, None)
+    o, lse = run(case)
+    assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+    case = W.attention(23, 2, 1, 400, 150, 128, True, None)   # causal, Nq > Nk
+    o, lse = run(case)
+    check(o, lse, *oracle_of(case))
+    assert torch.all(torch.isneginf(lse[:, :, :250]))
+
+
+def test_masked_keys_contribute_exactly_zero(cuda_ok):
+    """Keys past key_len hold two different finite garbage patterns; O and LSE
+    must be bitwise identical (and the causal future likewise)."""
+    B, H, N = 2, 2, 700
+    case = W.attention(24, B, H, N, N, 128, True, (200, 650))
+    outs = []
+    for pattern in range(2):
+        k, v = case.k.clone(), case.v.clone()
+        for b in range(B):
+            L = int(case.key_len[b])
+            if pattern == 0:
+                k[b, :, L:] = 1e30
+                v[b, :, L:] = -1e30
+            else:
+                g = torch.Generator().manual_seed(b)
+                k[b, :, L:] = (torch.randn(k[b, :, L:].shape, generator=g) * 100).to(torch.bfloat16)
+                v[b, :, L:] = (torch.randn(v[b, :, L:].shape, generator=g) * 100).to(torch.bfloat16)
+        c2 = W.AttnCase(case.q, k, v, case.scale, True, case.key_len)
+        outs.append(run(c2))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    check(*outs[0], *oracle_of(case))
+
+
+def test_deterministic(cuda_ok):
+    case = W.attention(25, 2, 4, 1000, 1000, 128, True, (500, 1000))
+    a, b = run(case), run(case)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def _sample_rows(N, key_len, rng, n=96):
+    rows = set(rng.choice(N, size=n, replace=False).tolist())
+    rows |= {0, 1, 2, 127, 128, 255, 256, N - 1}
+    if key_len is not None:
+        rows |= {max(0, int(key_len) - 2), min(N - 1, int(key_len)), min(N - 1, int(key_len) + 1)}
+    return np.array(sorted(rows))
+
+
+def test_full_size_noncausal(cuda_ok):
+    """B4 H16 N4096 d128, non-causal: every row of 4 heads vs the oracle."""
+    case = W.attn()
+    o, lse = run(case)
+    rng = np.random.default_rng(3)
+    for b, h in [(0, 0), (1, 7), (2, 15), (3, 3)]:
+        rows = _sample_rows(4096, None, rng, n=512)
+        (ro, rl), = oracle_of(case, rows=rows, bh=[(b, h)])
+        idx = torch.as_tensor(rows, device=o.device)
+        check(o[b:b + 1, h:h + 1, idx], lse[b:b + 1, h:h + 1, idx], ro, rl)
+    assert torch.all(torch.isfinite(o)) and torch.all(torch.isfinite(lse))
+
+
+def test_full_size_causal_padded(cuda_ok):
+    """B8 H32 N8192 d128, causal, key_len ~ U[4096, 8192]: 8 heads including the
+    shortest and longest batch entries, sampled rows vs the oracle."""
+    case = W.attn_causal()
+    o, lse = run(case)
+    kl = case.key_len.numpy()
+    bs = sorted({int(np.argmin(kl)), int(np.argmax(kl)), 0, 7})
+    rng = np.random.default_rng(4)
+    pairs = [(b, h) for b in bs for h in (0, 31)]
+    for b, h in pairs:
+        rows = _sample_rows(8192, kl[b], rng, n=160)
+        (ro, rl), = oracle_of(case, rows=rows, bh=[(b, h)])
+        idx = torch.as_tensor(rows, device=o.device)
+        check(o[b:b + 1, h:h + 1, idx], lse[b:b + 1, h:h + 1, idx], ro, rl)
+    assert torch.all(torch.isfinite(o)) and torch.all(torch.isfinite(lse))
