@@ -1,0 +1,429 @@
+"""Benchmark of the exact online-softmax attention hot path on one GB300.
+
+One step = one pass of every hot-path operation over its synthetic workload:
+  attention forward  B8 H32 N8192 d128 bf16, causal, key_len ~ U[4096, 8192]
+  row softmax        4096 x 32768 fp32 (2*N(0,1), 1% of entries at +40)
+  split-KV decode    B64 H32 Nk32768 d128 bf16, 16 splits, key_len ~ U[1024, 32768],
+                     followed by the merge of the split summaries
+The JSON line's headline `value` is the attention forward's throughput
+(algorithmic TFLOP/s: 4*d per visible (query, key) pair, exponentials not
+counted); the softmax and decode throughputs (algorithmic GB/s) are reported
+under "components", each with its own roofline.  All inputs are larger than
+the 129 MB L2, so no flush runs between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl osm|reference]
+
+--impl reference times the float64 CPU oracle (the reference arm of this
+method) on a bounded sample of the same attention workload.
+Under torchrun each rank runs the same per-GPU work (weak scaling); rank 0
+prints the line with the maximum time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attn fwd TFLOPS & % BF16 tensor peak; softmax/decode GB/s & % HBM peak"
+ATTN_SRC = os.path.join(ROOT, "exact_tiled_attention_osm_gb300", "csrc", "attn_fwd.cu")
+
+# DRAM traffic of one attention launch on this workload from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
+# source it was captured on (sha256 of attn_fwd.cu); None until captured.
+ATTN_TRAFFIC = {"bytes_per_launch": None, "source_sha256": None}
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def sha256(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+# ----------------------------------------------------------------- algorithmic work
+
+def attn_flops(B, H, Nq, Nk, d, causal, key_len):
+    """4*d per visible (query, key) pair: 2*d for q.k and 2*d for p*v."""
+    tot = 0
+    for b in range(B):
+        L = min(max(int(key_len[b]) if key_len is not None else Nk, 0), Nk)
+        if causal:
+            off = Nk - Nq
+            i = np.arange(Nq, dtype=np.int64)
+            vis = np.clip(np.minimum(L, i + 1 + off), 0, None)
+            tot += int(vis.sum())
+        else:
+            tot += L * Nq
+    return 4 * d * H * tot
+
+
+def decode_bytes(B, H, d, key_len, elem=2):
+    keys = sum(int(x) for x in key_len)
+    return H * keys * d * elem * 2 + B * H * d * elem * 2 + B * H * 4
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons, power = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ----------------------------------------------------------------- the GPU arm
+
+class Workloads:
+    def __init__(self, dev):
+        import workloads as W
+        t0 = time.time()
+        self.attn = W.attn_causal()
+        a = self.attn
+        self.q, self.k, self.v = a.q.to(dev), a.k.to(dev), a.v.to(dev)
+        self.kl = a.key_len.to(dev)
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty(a.q.shape[:3], dtype=torch.float32, device=dev)
+        B, H, N, d = a.q.shape
+        self.attn_flops = attn_flops(B, H, N, N, d, True, a.key_len.numpy())
+        x = W.softmax_logits(2)
+        self.x = x.to(dev)
+        self.y = torch.empty_like(self.x)
+        self.softmax_bytes = 8 * x.numel()
+        dc = W.decode(5, device=str(dev))
+        self.dec = dc
+        from exact_tiled_attention_osm_gb300 import decode_workspace_bytes
+        Bd, Hd, _, dd = dc.q.shape
+        self.ws = torch.empty(decode_workspace_bytes(Bd, Hd, dd, dc.num_splits), dtype=torch.uint8,
+                              device=dev)
+        self.od = torch.empty_like(dc.q)
+        self.ld = torch.empty((Bd, Hd), dtype=torch.float32, device=dev)
+        self.decode_bytes = decode_bytes(Bd, Hd, dd, dc.key_len.cpu().numpy())
+        self.setup_s = time.time() - t0
+
+
+def gpu_arm(args, rank, world, dev):
+    import exact_tiled_attention_osm_gb300 as osm
+    osm.load_library()
+    wl = Workloads(dev)
+    stream = torch.cuda.current_stream(dev)
+    dc = wl.dec
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        osm.attn_fwd(wl.q, wl.k, wl.v, wl.attn.scale, True, wl.kl, out=wl.o, lse=wl.lse)
+        if ev is not None:
+            ev[1].record(stream)
+        osm.softmax_rows(wl.x, out=wl.y)
+        if ev is not None:
+            ev[2].record(stream)
+        osm.attn_decode_splitkv(dc.q, dc.k, dc.v, dc.scale, dc.key_len, dc.num_splits,
+                                workspace=wl.ws, out=wl.od, lse=wl.ld)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if osm.device_status() != 0:
+        raise RuntimeError("a device-side wait ran out during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clk = ClockSampler(dev.index if dev.index is not None else 0)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clk.start()
+    time.sleep(0.3)  # let the sampler take its first reading
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = clk.stop()
+    total_ms = start.elapsed_time(end)
+    t_attn = [e[0].elapsed_time(e[1]) for e in evs]
+    t_soft = [e[1].elapsed_time(e[2]) for e in evs]
+    t_dec = [e[2].elapsed_time(e[3]) for e in evs]
+    if osm.device_status() != 0:
+        raise RuntimeError("a device-side wait ran out during the timed region")
+
+    # end to end through the public API with host buffers: H2D of the step's
+    # attention inputs from pinned memory, the call, D2H of O and LSE
+    hq, hk, hv = (t.pin_memory() for t in (wl.attn.q, wl.attn.k, wl.attn.v))
+    hkl = wl.attn.key_len.pin_memory()
+    ho = torch.empty(wl.o.shape, dtype=wl.o.dtype, pin_memory=True)
+    hl = torch.empty(wl.lse.shape, dtype=wl.lse.dtype, pin_memory=True)
+    dq, dk, dv = torch.empty_like(wl.q), torch.empty_like(wl.k), torch.empty_like(wl.v)
+    dkl = torch.empty_like(wl.kl)
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        dkl.copy_(hkl, non_blocking=True)
+        o, lse = osm.attn_fwd(dq, dk, dv, wl.attn.scale, True, dkl, out=wl.o, lse=wl.lse)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hkl))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    del hq, hk, hv, ho, hl, dq, dk, dv
+
+    res = {
+        "total_ms": total_ms,
+        "attn_ms": statistics.mean(t_attn),
+        "soft_ms": statistics.mean(t_soft),
+        "dec_ms": statistics.mean(t_dec),
+        "e2e_ms": e2e_ms,
+        "h2d": h2d, "d2h": d2h,
+        "clocks": clocks,
+        "setup_s": wl.setup_s,
+        "attn_flops": wl.attn_flops,
+        "softmax_bytes": wl.softmax_bytes,
+        "decode_bytes": wl.decode_bytes,
+    }
+    return res
+
+
+def cpu_oracle_sample(budget_s=12.0, seed_rows=0):
+    """Time the float64 oracle on (b, h) heads of the attention workload, 1024
+    query rows each, until `budget_s` of CPU time is spent.  Returns
+    (TFLOP/s, description, threads)."""
+    import oracle
+    import workloads as W
+    B, H, N, d = 8, 32, 8192, 128
+    lens = W.key_lengths(4, B, 4096, 8192)
+    rng = np.random.default_rng(seed_rows)
+    flops, t_used, heads = 0, 0.0, 0
+    # generate one head at a time (the oracle's inputs are the same bf16 values)
+    for idx in range(B * H):
+        b, h = divmod((idx * 37) % (B * H), H)
+        part = b * H + h
+        q = W.to_bf16(W.normal_f32(4, 1, (N, d), part=part))
+        k = W.to_bf16(W.normal_f32(4, 2, (N, d), part=part))
+        v = W.to_bf16(W.normal_f32(4, 3, (N, d), part=part))
+        rows = np.sort(rng.choice(N, size=1024, replace=False))
+        q64, k64, v64 = (W.as_f64(t)[None, None] for t in (q, k, v))
+        t0 = time.perf_counter()
+        oracle.attention_ref(q64, k64, v64, 1 / math.sqrt(d), True, [int(lens[b])], rows=rows)
+        t_used += time.perf_counter() - t0
+        L = int(lens[b])
+        flops += 4 * d * int(np.minimum(L, rows + 1).sum())
+        heads += 1
+        if t_used >= budget_s:
+            break
+    desc = (f"{heads} (b,h) heads x 1024 sampled query rows of the causal+padding "
+            f"B8 H32 N8192 d128 workload, all their visible keys")
+    return flops / t_used / 1e12, desc, t_used
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(n[0])
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+TIME_KEYS = ("total_ms", "attn_ms", "soft_ms", "dec_ms", "e2e_ms")
+
+
+def reduce_max(times: dict, world: int, device) -> dict:
+    """Element-wise maximum of a dict of times over all ranks (identity at world 1)."""
+    keys = sorted(times)
+    t = torch.tensor([float(times[k]) for k in keys], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return dict(zip(keys, t.tolist()))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="osm", choices=["osm", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pk, pk_kind = peaks()
+    config = {"workload": "attn fwd causal+padding B8 H32 N8192 d128 bf16 (key_len U[4096,8192]); "
+                          "softmax 4096x32768 fp32; decode B64 H32 Nk32768 d128 bf16 16 splits",
+              "attn": {"B": 8, "H": 32, "Nq": 8192, "Nk": 8192, "d": 128, "causal": True,
+                       "key_len": "U[4096,8192]", "scale": "1/sqrt(128)"},
+              "softmax": {"rows": 4096, "cols": 32768},
+              "decode": {"B": 64, "H": 32, "Nk": 32768, "d": 128, "num_splits": 16,
+                         "key_len": "U[1024,32768]"},
+              "l2": "inputs larger than L2 (129 MB); no flush between steps",
+              "parallelism": f"replicas x{args.gpus}"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        tf, desc, used = cpu_oracle_sample(args.cpu_budget)
+        cores = blas_threads()
+        line = {"impl": "reference", "metric": METRIC, "value": tf, "unit": "TFLOP/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+                "config": config,
+                "cpu_baseline": {"value": tf, "unit": "TFLOP/s", "cores": cores,
+                                 "kind": "oracle", "sample": desc},
+                "e2e": {"value": tf, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (libosm has no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    res = gpu_arm(args, rank, world, dev)
+
+    # max over ranks of every time; per-GPU work is identical (weak scaling)
+    mx = reduce_max({k: res[k] for k in TIME_KEYS}, world, dev)
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    attn_tf = world * res["attn_flops"] / (mx["attn_ms"] * 1e-3) / 1e12
+    soft_gbs = world * res["softmax_bytes"] / (mx["soft_ms"] * 1e-3) / 1e9
+    dec_gbs = world * res["decode_bytes"] / (mx["dec_ms"] * 1e-3) / 1e9
+    per_gpu_tf = attn_tf / world
+    src_sha = sha256(ATTN_SRC)
+    traffic = (ATTN_TRAFFIC["bytes_per_launch"]
+               if ATTN_TRAFFIC["source_sha256"] == src_sha else None)
+    peak_tc = pk["bf16_tflops"]
+    roofline = {"bound": "tensor", "achieved": per_gpu_tf, "peak": peak_tc, "unit": "TFLOP/s",
+                "frac": per_gpu_tf / peak_tc, "traffic": traffic,
+                "peak_kind": f"{pk_kind} bf16 burst",
+                "frac_of_sustained": per_gpu_tf / pk.get("bf16_tflops_sustained", peak_tc),
+                "kernel": "attn_fwd_kernel", "per_launch_flops": res["attn_flops"],
+                "avg_launch_ms": mx["attn_ms"]}
+    hbm = pk["hbm_gbs"]
+    components = {
+        "softmax_rows": {"value": soft_gbs, "unit": "GB/s", "ms": mx["soft_ms"],
+                         "roofline": {"bound": "hbm", "achieved": soft_gbs / world, "peak": hbm,
+                                      "unit": "GB/s", "frac": soft_gbs / world / hbm,
+                                      "traffic": None, "per_launch_bytes": res["softmax_bytes"],
+                                      "peak_kind": f"{pk_kind} copy"}},
+        "decode_splitkv": {"value": dec_gbs, "unit": "GB/s", "ms": mx["dec_ms"],
+                           "roofline": {"bound": "hbm", "achieved": dec_gbs / world, "peak": hbm,
+                                        "unit": "GB/s", "frac": dec_gbs / world / hbm,
+                                        "traffic": None,
+                                        "per_launch_bytes": res["decode_bytes"],
+                                        "peak_kind": f"{pk_kind} copy",
+                                        "note": "split kernel + merge kernel, one pass"}},
+    }
+    e2e_tf = world * res["attn_flops"] / (mx["e2e_ms"] * 1e-3) / 1e12
+    line = {"metric": METRIC, "value": attn_tf, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": mx["total_ms"] / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded, generated on the host)", "config": config,
+            "roofline": roofline, "components": components,
+            "e2e": {"value": e2e_tf, "unit": "TFLOP/s", "h2d_bytes_per_step": res["h2d"],
+                    "d2h_bytes_per_step": res["d2h"], "ms_per_step": mx["e2e_ms"],
+                    "what": "attention forward via the public API from pinned host buffers"},
+            "gpu_launches": 4 * args.steps,
+            "clocks": res["clocks"]}
+    if not args.no_cpu_baseline and world == 1:
+        tf, desc, used = cpu_oracle_sample(args.cpu_budget)
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": blas_threads(),
+                                "kind": "oracle", "sample": desc, "seconds": used}
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -232,11 +232,10 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ mp
 #pragma unroll
   for (int e = 0; e < PER; ++e) o[e] = 0.f;
   if (M != kNegInf) {
-    const float Mb = M * kLog2e;
     for (int s = 0; s < S; ++s) {
       const float ms = mpart[s * rows + row];
       if (ms == kNegInf) continue;
-      const float w = ptx::ex2(fmaf(ms, kLog2e, -Mb));
+      const float w = ptx::ex2((ms - M) * kLog2e);
       l = fmaf(TRIPLE ? lpart[s * rows + row] : 1.f, w, l);
       const float* src = opart + (s * rows + row) * D + lane * PER;
 #pragma unroll

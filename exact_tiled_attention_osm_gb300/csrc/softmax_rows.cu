@@ -122,13 +122,13 @@ __global__ void __launch_bounds__(kThreads) softmax_rows_cluster(const float* __
   float m = kNegInf;
 #pragma unroll
   for (int i = 0; i < V; ++i) m = fmaxf(m, fmaxf(fmaxf(v[i].x, v[i].y), fmaxf(v[i].z, v[i].w)));
+  // (x - m) first: exact near the max whatever the magnitude of m
   float l = 0.f;
   if (m != kNegInf) {
-    const float mb = m * kLog2e;
 #pragma unroll
     for (int i = 0; i < V; ++i) {
-      l += ptx::ex2(fmaf(v[i].x, kLog2e, -mb)) + ptx::ex2(fmaf(v[i].y, kLog2e, -mb)) +
-           ptx::ex2(fmaf(v[i].z, kLog2e, -mb)) + ptx::ex2(fmaf(v[i].w, kLog2e, -mb));
+      l += ptx::ex2((v[i].x - m) * kLog2e) + ptx::ex2((v[i].y - m) * kLog2e) +
+           ptx::ex2((v[i].z - m) * kLog2e) + ptx::ex2((v[i].w - m) * kLog2e);
     }
   }
   // warp tree
@@ -192,10 +192,9 @@ __global__ void __launch_bounds__(kGenThreads) softmax_rows_generic(const float*
     const float mt = fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3]));
     if (mt == kNegInf) continue;
     const float mn = fmaxf(m, mt);
-    const float mb = mn * kLog2e;
     float s = 0.f;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) s += ptx::ex2(fmaf(a[u], kLog2e, -mb));
+    for (int u = 0; u < 4; ++u) s += ptx::ex2((a[u] - mn) * kLog2e);
     l = l * rebase(m, mn) + s;
     m = mn;
   }
