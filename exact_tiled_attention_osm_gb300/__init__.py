@@ -37,6 +37,7 @@ SIGNATURES = {
     "osm_attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P]),
     "osm_attn_decode_splitkv_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "osm_attn_decode_splitkv": (_I, [_I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _I, _P, _SZ, _P]),
+    "osm_attn_decode_splitkv_noalloc": (_I, [_I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _I, _P]),
     "osm_lse_merge": (_I, [_P, _P, _I, _I64, _I, _I, _P, _P, _P]),
     "osm_status_string": (ctypes.c_char_p, [_I]),
     "osm_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint32)]),
@@ -184,6 +185,47 @@ def attn_decode_splitkv(q, k, v, scale=None, key_len=None, num_splits=16, worksp
                                            float(scale), kl, int(num_splits),
                                            workspace.data_ptr(), workspace.numel(), _stream(q)),
                "osm_attn_decode_splitkv")
+    return o, lse_t
+
+
+# bytes of the library's own scratch area used by attn_decode_splitkv_noalloc
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def attn_decode_splitkv_noalloc(q, k, v, scale=None, key_len=None, num_splits=16, out=None,
+                                lse=None):
+    """Split-KV decode that allocates nothing on the device inside the library.
+
+    For callers that cannot allocate device memory (for example a plug-in whose
+    host program owns all device memory): the split summaries live in a fixed
+    scratch area of NOALLOC_SCRATCH_BYTES inside libosm, shared by every call on
+    the device, so calls must not overlap on the GPU.  Output tensors are
+    allocated here only when `out` / `lse` are not given.
+    """
+    dt = {torch.bfloat16: OSM_BF16, torch.float32: OSM_F32}.get(q.dtype)
+    if dt is None:
+        raise ValueError("decode supports bf16 and fp32")
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype, q.device)
+    B, H, one, d = q.shape
+    if one != 1 or k.dim() != 4 or v.shape != k.shape or k.shape[0] != B or k.shape[1] != H \
+            or k.shape[3] != d:
+        raise ValueError("q must be [B,H,1,d] and k, v [B,H,Nk,d]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q) if out is None else out
+    lse_t = torch.empty((B, H), dtype=torch.float32, device=q.device) if lse is None else lse
+    kl = 0
+    if key_len is not None:
+        _need(key_len, "key_len", torch.int32, q.device)
+        kl = key_len.data_ptr()
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        _check(lib.osm_attn_decode_splitkv_noalloc(dt, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                                   o.data_ptr(), lse_t.data_ptr(), B, H,
+                                                   k.shape[2], d, float(scale), kl,
+                                                   int(num_splits), _stream(q)),
+               "osm_attn_decode_splitkv_noalloc")
     return o, lse_t
 
 

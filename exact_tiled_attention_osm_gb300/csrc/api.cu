@@ -93,6 +93,29 @@ osm_status osm_attn_decode_splitkv(osm_dtype dt, const void* q, const void* k, c
                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
+osm_status osm_attn_decode_splitkv_noalloc(osm_dtype dt, const void* q, const void* k,
+                                           const void* v, void* o, float* lse, int B, int H,
+                                           int Nk, int d, float scale, const int32_t* key_len,
+                                           int num_splits, osm_stream_t stream) {
+  if (dt != OSM_F32 && dt != OSM_BF16) return OSM_ERR_INVALID_VALUE;
+  if (B < 0 || H < 0 || Nk < 0) return OSM_ERR_INVALID_VALUE;
+  if (d != 64 && d != 128) return (d > 0) ? OSM_ERR_UNSUPPORTED : OSM_ERR_INVALID_VALUE;
+  if (num_splits < 1 || num_splits > 256) return OSM_ERR_INVALID_VALUE;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return OSM_ERR_INVALID_VALUE;
+  if (static_cast<int64_t>(B) * H == 0) return OSM_OK;
+  if (B > 65535 || H > 65535) return OSM_ERR_UNSUPPORTED;
+  // the summaries must fit the library's fixed scratch area
+  if (osm::decode_workspace_bytes(B, H, d, num_splits) > OSM_NOALLOC_SCRATCH_BYTES)
+    return OSM_ERR_INVALID_VALUE;
+  if (!q || !o || !lse || (Nk > 0 && (!k || !v))) return OSM_ERR_INVALID_VALUE;
+  if (!aligned16(q) || !aligned16(o) || !aligned4(lse)) return OSM_ERR_INVALID_VALUE;
+  if (Nk > 0 && (!aligned16(k) || !aligned16(v))) return OSM_ERR_INVALID_VALUE;
+  if (key_len && !aligned4(key_len)) return OSM_ERR_INVALID_VALUE;
+  return from_cuda(osm::launch_decode_splitkv_noalloc(dt, q, k, v, o, lse, B, H, Nk, d, scale,
+                                                      key_len, num_splits,
+                                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
 osm_status osm_lse_merge(const float* o_parts, const float* lse_parts, int S, int64_t rows, int d,
                          osm_dtype out_dt, void* o, float* lse, osm_stream_t stream) {
   if (out_dt != OSM_F32 && out_dt != OSM_BF16) return OSM_ERR_INVALID_VALUE;

@@ -21,6 +21,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -313,6 +314,47 @@ cudaError_t launch_decode_splitkv(osm_dtype dt, const void* q, const void* k, co
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_merge<true>(ws.m, ws.l, ws.o, S, rows, d, dt, o, lse, s);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode.  Callers that cannot allocate device memory get the
+// split summaries kept in this fixed-size device array instead of a workspace
+// of their own.  Host code must not hand the array's name to a kernel (on the
+// host it is only a stand-in symbol, not a device address): the device
+// address is looked up once per device with cudaGetSymbolAddress and cached.
+namespace {
+static __device__ __align__(256) unsigned char g_noalloc_scratch[OSM_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxCachedDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxCachedDevices] = {};
+
+cudaError_t noalloc_scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (dev >= 0 && dev < kMaxCachedDevices && g_noalloc_ptr[dev] != nullptr) {
+    *out = g_noalloc_ptr[dev];
+    return cudaSuccess;
+  }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // the current device's copy
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kMaxCachedDevices) g_noalloc_ptr[dev] = p;
+  *out = p;
+  return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t launch_decode_splitkv_noalloc(osm_dtype dt, const void* q, const void* k,
+                                          const void* v, void* o, float* lse, int B, int H,
+                                          int Nk, int d, float scale, const int32_t* key_len,
+                                          int S, cudaStream_t s) {
+  void* scratch = nullptr;
+  cudaError_t e = noalloc_scratch_address(&scratch);
+  if (e != cudaSuccess) return e;
+  return launch_decode_splitkv(dt, q, k, v, o, lse, B, H, Nk, d, scale, key_len, S, scratch, s);
 }
 
 cudaError_t launch_lse_merge(const float* o_parts, const float* lse_parts, int S, int64_t rows,

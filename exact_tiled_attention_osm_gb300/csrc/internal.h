@@ -25,6 +25,11 @@ size_t decode_workspace_bytes(int B, int H, int d, int S);
 cudaError_t launch_decode_splitkv(osm_dtype dt, const void* q, const void* k, const void* v,
                                   void* o, float* lse, int B, int H, int Nk, int d, float scale,
                                   const int32_t* key_len, int S, void* ws, cudaStream_t s);
+// the same decode, with the summaries in the library's own scratch area
+cudaError_t launch_decode_splitkv_noalloc(osm_dtype dt, const void* q, const void* k,
+                                          const void* v, void* o, float* lse, int B, int H,
+                                          int Nk, int d, float scale, const int32_t* key_len,
+                                          int S, cudaStream_t s);
 cudaError_t launch_lse_merge(const float* o_parts, const float* lse_parts, int S, int64_t rows,
                              int d, osm_dtype out_dt, void* o, float* lse, cudaStream_t s);
 

@@ -159,6 +159,47 @@ osm_status osm_attn_decode_splitkv(osm_dtype dt, const void *q, const void *k, c
 osm_status osm_lse_merge(const float *o_parts, const float *lse_parts, int S, int64_t rows,
                          int d, osm_dtype out_dt, void *o, float *lse, osm_stream_t stream);
 
+/*
+ * OSM_NOALLOC_SCRATCH_BYTES — size of the device scratch area that libosm
+ * reserves (as a fixed-size device array, on every GPU that loads the library,
+ * until the process exits) for osm_attn_decode_splitkv_noalloc.
+ */
+#define OSM_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/*
+ * osm_attn_decode_splitkv_noalloc — osm_attn_decode_splitkv for callers that
+ * cannot allocate device memory.  The pages have no counterpart; this entry
+ * point exists for the caller, not for the method.
+ *
+ * Some callers cannot call cudaMalloc: a plug-in loaded into a host program
+ * that owns every byte of device memory and hands its plug-ins no allocator,
+ * or code that runs under a fixed device-memory budget where allocating after
+ * start-up is forbidden.  Such a caller cannot provide the split summaries'
+ * workspace, so this entry point keeps them in a scratch area inside the
+ * library instead (OSM_NOALLOC_SCRATCH_BYTES, reserved when the library's
+ * device code is loaded).  It calls no allocator of any kind.
+ *
+ * Arguments, layouts, results and errors are those of osm_attn_decode_splitkv
+ * without `workspace` / `workspace_bytes`.  In addition it returns
+ * OSM_ERR_INVALID_VALUE, launching nothing, when the summaries would need more
+ * than OSM_NOALLOC_SCRATCH_BYTES, i.e. when
+ * osm_attn_decode_splitkv_workspace_bytes(B, H, d, num_splits) is larger.
+ *
+ * The first call on a device looks up the scratch area's device address
+ * (with that device current) and caches it; make that first call before any
+ * stream capture begins.
+ * Every call on a device shares the one scratch area, which keeps the last
+ * call's summaries; nothing in it needs to start at zero, because the split
+ * kernel writes every summary slot that the merge kernel reads.  Calls whose
+ * work overlaps on the GPU (on different streams, or from different threads)
+ * race on the scratch area and give undefined results: order them on one
+ * stream or synchronise between them.
+ */
+osm_status osm_attn_decode_splitkv_noalloc(osm_dtype dt, const void *q, const void *k,
+                                           const void *v, void *o, float *lse, int B, int H,
+                                           int Nk, int d, float scale, const int32_t *key_len,
+                                           int num_splits, osm_stream_t stream);
+
 /* Text for a status code (static storage; never NULL). */
 const char *osm_status_string(osm_status status);
 
