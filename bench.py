@@ -317,6 +317,58 @@ def reduce_max(times: dict, world: int, device) -> dict:
     return dict(zip(keys, t.tolist()))
 
 
+def profile_case(spec: str, iters: int):
+    """Run one operation `iters` times on a given shape (for ncu captures).
+
+    spec: "attn:B,H,N[,causal]" | "softmax:rows,cols" | "decode:B,H,Nk[,splits]".
+    Inputs come from the same generators as the full workloads.
+    """
+    import exact_tiled_attention_osm_gb300 as osm
+    import workloads as W
+    op, _, arg = spec.partition(":")
+    parts = arg.split(",")
+    dev = torch.device("cuda", 0)
+    if op == "attn":
+        B, H, N = (int(x) for x in parts[:3])
+        causal = len(parts) > 3 and parts[3] == "causal"
+        c = W.attention(4, B, H, N, N, 128, causal, (N // 2, N) if causal else None)
+        q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
+        kl = c.key_len.to(dev) if c.key_len is not None else None
+        run = lambda: osm.attn_fwd(q, k, v, c.scale, causal, kl)
+        work = attn_flops(B, H, N, N, 128, causal, None if kl is None else c.key_len.numpy())
+        unit = "TFLOP/s"
+    elif op == "softmax":
+        R, C = (int(x) for x in parts[:2])
+        x = W.softmax_logits(2, rows=R, cols=C).to(dev)
+        y = torch.empty_like(x)
+        run = lambda: osm.softmax_rows(x, out=y)
+        work, unit = 8 * R * C, "GB/s"
+    elif op == "decode":
+        B, H, Nk = (int(x) for x in parts[:3])
+        S = int(parts[3]) if len(parts) > 3 else 16
+        dc = W.decode(5, B=B, H=H, Nk=Nk, len_range=(Nk // 32, Nk), num_splits=S, device="cuda")
+        ws = torch.empty(osm.decode_workspace_bytes(B, H, 128, S), dtype=torch.uint8, device=dev)
+        run = lambda: osm.attn_decode_splitkv(dc.q, dc.k, dc.v, dc.scale, dc.key_len, S,
+                                              workspace=ws)
+        work, unit = decode_bytes(B, H, 128, dc.key_len.cpu().numpy()), "GB/s"
+    else:
+        raise SystemExit(f"unknown op {op}")
+    run()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * iters)]
+    for i in range(iters):
+        ev[2 * i].record()
+        run()
+        ev[2 * i + 1].record()
+    torch.cuda.synchronize()
+    if osm.device_status() != 0:
+        raise RuntimeError("a device-side wait ran out")
+    ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(iters)]
+    scale = 1e12 if unit == "TFLOP/s" else 1e9
+    print(json.dumps({"profile": spec, "iters": iters, "ms": ms,
+                      "best": work / (min(ms) * 1e-3) / scale, "unit": unit, "work": work}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -325,7 +377,14 @@ def main():
     ap.add_argument("--impl", default="osm", choices=["osm", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", default=None,
+                    help="run one op on a given shape instead of the benchmark, e.g. "
+                         "attn:2,16,8192,causal | softmax:1024,32768 | decode:4,32,32768")
+    ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
+    if args.profile:
+        profile_case(args.profile, args.iters)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 
