@@ -21,9 +21,13 @@
 //   warp 1     MMA issuer (one thread): S_t = Q_t K_j^T into TMEM, then
 //              O~_t += P_t V_j with P_t read straight from TMEM.
 //   warps 4-7  softmax for query tile 0; warps 8-11 for tile 1.  One thread
-//              per query row: TMEM -> registers, mask, row max, exp2, row sum,
-//              P as bf16 back into TMEM over S, rescale O~ in TMEM when the
-//              max has grown, and the final O = O~ / l, lse epilogue.
+//              per query row.  Pass 1: the row's 128 scores TMEM -> registers,
+//              mask, row max.  Pass 2, a rolled loop over four 32-column
+//              chunks (small code, no register spills): reload the chunk from
+//              TMEM, scale and subtract in packed f32x2, 32 independent exp2
+//              (so the MUFU latency is covered), row sum, bf16 pack, store P
+//              over the S columns already consumed.  Rescale O~ in TMEM when
+//              the max has grown; epilogue O = O~ / l, lse.
 //   TMEM       512 columns: S_0 | S_1 | O~_0 | O~_1 (128 fp32 columns each).
 // The rescale is taken only when the new max exceeds the reference by more
 // than kTau (base-2 units); every identity of the recurrence holds for any
@@ -121,6 +125,8 @@ __device__ __forceinline__ Item item_info(const Params& p, int item) {
 
 __device__ unsigned int g_err_word;
 
+// ---- experiment switches (defaults = committed design) ----
+
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -161,139 +167,147 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  if (warp == 0 && lane == 0) {
-    // ------------------------------------------------------------ TMA producer
-    prefetch_tmap(&tm_q);
-    prefetch_tmap(&tm_k);
-    prefetch_tmap(&tm_v);
-    uint32_t slot = 0, ph = 0, qe_ph = 0;
-    uint32_t fill_mask = 0, fill_ph = 0;  // slots ever filled / parity of their last fill
-    int q_fill = -1;
-    int loaded = 0;
-    bool ok = true;
-    for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x) {
-      const Item it = item_info(p, item);
-      if (it.n_kv == 0) continue;
-      if (loaded > 0) {
-        if (!(ok = wait_bounded(bar(Q_EMPTY), qe_ph, abort_flag, p.err, kSite | 1))) break;
-        qe_ph ^= 1;
-      }
-      for (int t = 0; t < 2; ++t) {
-        mbar_arrive_expect_tx(bar(Q_FULL + t), kTileBytes);
-        for (int c = 0; c < 2; ++c)
-          tma_load_3d(sQ + t * kTileBytes + c * kBoxBytes, &tm_q, bar(Q_FULL + t), c * 64,
-                      it.q0 + t * kRows, it.bh);
-      }
-      q_fill = loaded & 1;
-      ++loaded;
-      for (int j = 0; ok && j < it.n_kv; ++j) {
-        for (int kv = 0; kv < 2; ++kv) {
-          if (!(ok = wait_bounded(bar(KV_EMPTY + slot), ph ^ 1, abort_flag, p.err, kSite | 2)))
-            break;
-          mbar_arrive_expect_tx(bar(KV_FULL + slot), kTileBytes);
-          const CUtensorMap* tm = kv ? &tm_v : &tm_k;
+  // a wait of a group of lanes: every lane polls; with a whole warp the lanes agree
+  // bounded waits: by one thread, or by a whole warp that then agrees on the outcome
+  auto wait_one = [&](uint32_t b, uint32_t parity, unsigned site) -> bool {
+    return wait_bounded(b, parity, abort_flag, p.err, site);
+  };
+  auto wait_all = [&](uint32_t b, uint32_t parity, unsigned site) -> bool {
+    return __all_sync(0xffffffffu, wait_bounded(b, parity, abort_flag, p.err, site));
+  };
+
+  if (warp < 4) {
+    if (warp == 0 && lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      uint32_t slot = 0, ph = 0, qe_ph = 0;
+      uint32_t fill_mask = 0, fill_ph = 0;
+      int q_fill = -1;
+      int loaded = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x) {
+        const Item it = item_info(p, item);
+        if (it.n_kv == 0) continue;
+        if (loaded > 0) {
+          if (!(ok = wait_one(bar(Q_EMPTY), qe_ph, kSite | 1))) break;
+          qe_ph ^= 1;
+        }
+        for (int t = 0; t < 2; ++t) {
+          mbar_arrive_expect_tx(bar(Q_FULL + t), kTileBytes);
           for (int c = 0; c < 2; ++c)
-            tma_load_3d(sKV + slot * kTileBytes + c * kBoxBytes, tm, bar(KV_FULL + slot), c * 64,
-                        j * kKeys, it.bh);
-          fill_mask |= 1u << slot;
-          fill_ph = (fill_ph & ~(1u << slot)) | (ph << slot);
-          if (++slot == kSlots) {
-            slot = 0;
-            ph ^= 1;
+            tma_load_3d(sQ + t * kTileBytes + c * kBoxBytes, &tm_q, bar(Q_FULL + t), c * 64,
+                        it.q0 + t * kRows, it.bh);
+        }
+        q_fill = loaded & 1;
+        ++loaded;
+        for (int j = 0; ok && j < it.n_kv; ++j) {
+          for (int kv = 0; kv < 2; ++kv) {
+            if (!(ok = wait_one(bar(KV_EMPTY + slot), ph ^ 1, kSite | 2))) break;
+            mbar_arrive_expect_tx(bar(KV_FULL + slot), kTileBytes);
+            const CUtensorMap* tm = kv ? &tm_v : &tm_k;
+            for (int c = 0; c < 2; ++c)
+              tma_load_3d(sKV + slot * kTileBytes + c * kBoxBytes, tm, bar(KV_FULL + slot),
+                          c * 64, j * kKeys, it.bh);
+            fill_mask |= 1u << slot;
+            fill_ph = (fill_ph & ~(1u << slot)) | (ph << slot);
+            if (++slot == kSlots) {
+              slot = 0;
+              ph ^= 1;
+            }
           }
         }
       }
-    }
-    if (!ok) {  // let every copy this thread started land before the CTA exits
-      for (int s = 0; s < kSlots; ++s)
-        if (fill_mask >> s & 1u) wait_drain(bar(KV_FULL + s), fill_ph >> s & 1u, 200000000ull);
-      if (q_fill >= 0)
-        for (int t = 0; t < 2; ++t) wait_drain(bar(Q_FULL + t), q_fill, 200000000ull);
-    }
-  } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------------------ MMA issuer
-    uint32_t slot = 0, ph = 0, qf_ph = 0;
-    uint32_t pf_ph[2] = {0, 0}, oe_ph[2] = {0, 0};
-    int done = 0;
-    bool ok = true;
-    const uint64_t dK = sdesc_sw128(0, 16, 1024);       // K-major template (address added)
-    const uint64_t dV = sdesc_sw128(0, 16384, 1024);    // MN-major template
-    for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x) {
-      const Item it = item_info(p, item);
-      if (it.n_kv == 0) continue;
-      if (!(ok = wait_bounded(bar(Q_FULL), qf_ph, abort_flag, p.err, kSite | 3))) break;
-      if (!(ok = wait_bounded(bar(Q_FULL + 1), qf_ph, abort_flag, p.err, kSite | 3))) break;
-      qf_ph ^= 1;
-      tc_fence_after();
-      bool first_pv[2] = {true, true};
-      uint32_t v_slot = 0, v_ph = 0;
-      // P_t V_{j-1} for tile t (waits for the softmax of tile t)
-      auto issue_pv = [&](int t) -> bool {
-        if (!wait_bounded(bar(P_FULL + t), pf_ph[t], abort_flag, p.err, kSite | 5)) return false;
-        pf_ph[t] ^= 1;
-        if (first_pv[t] && done > 0) {
-          if (!wait_bounded(bar(O_EMPTY + t), oe_ph[t], abort_flag, p.err, kSite | 6))
-            return false;
-          oe_ph[t] ^= 1;
-        }
+      if (!ok) {  // let every copy this thread started land before the CTA exits
+        for (int s = 0; s < kSlots; ++s)
+          if (fill_mask >> s & 1u) wait_drain(bar(KV_FULL + s), fill_ph >> s & 1u, 200000000ull);
+        if (q_fill >= 0)
+          for (int t = 0; t < 2; ++t) wait_drain(bar(Q_FULL + t), q_fill, 200000000ull);
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      uint32_t slot = 0, ph = 0, qf_ph = 0;
+      uint32_t pf_ph[2] = {0, 0}, oe_ph[2] = {0, 0};
+      int done = 0;
+      bool ok = true;
+      const uint64_t dK = sdesc_sw128(0, 16, 1024);     // K-major template (address added)
+      const uint64_t dV = sdesc_sw128(0, 16384, 1024);  // MN-major template
+      for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x) {
+        const Item it = item_info(p, item);
+        if (it.n_kv == 0) continue;
+        for (int t = 0; t < 2 && ok; ++t) ok = wait_one(bar(Q_FULL + t), qf_ph, kSite | 3);
+        if (!ok) break;
+        qf_ph ^= 1;
         tc_fence_after();
-        const uint32_t vaddr = sKV + v_slot * kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {
-          mma_ts(tbase + kTmemO + t * 128, tbase + kTmemS + t * 128 + kk * 8,
-                 dV + ((vaddr + kk * 2048) >> 4), kIdescPV, (!first_pv[t] || kk > 0) ? 1u : 0u);
-        }
-        first_pv[t] = false;
-        return true;
-      };
-      for (int j = 0; ok && j < it.n_kv; ++j) {
-        const uint32_t k_slot = slot;
-        if (!(ok = wait_bounded(bar(KV_FULL + k_slot), ph, abort_flag, p.err, kSite | 4))) break;
-        if (++slot == kSlots) { slot = 0; ph ^= 1; }
-        const uint32_t nv_slot = slot, nv_ph = ph;
-        if (++slot == kSlots) { slot = 0; ph ^= 1; }
-        if (j > 0) {
-          if (!(ok = wait_bounded(bar(KV_FULL + v_slot), v_ph, abort_flag, p.err, kSite | 4)))
-            break;
-        }
-        tc_fence_after();
-        const uint32_t kaddr = sKV + k_slot * kTileBytes;
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (j > 0 && !(ok = issue_pv(t))) break;
-          const uint32_t qaddr = sQ + t * kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-            mma_ss(tbase + kTmemS + t * 128, dK + ((qaddr + off) >> 4), dK + ((kaddr + off) >> 4),
-                   kIdescS, kk > 0 ? 1u : 0u);
+        bool first_pv[2] = {true, true};
+        uint32_t v_slot = 0, v_ph = 0;
+        // O~_t += P_t V_{j-1} once the softmax of tile t has stored P_t
+        auto issue_pv = [&](int t) -> bool {
+          const uint64_t vdesc = dV + ((sKV + v_slot * kTileBytes) >> 4);
+          if (!wait_one(bar(P_FULL + t), pf_ph[t], kSite | 5)) return false;
+          if (first_pv[t] && done > 0) {
+            if (!wait_one(bar(O_EMPTY + t), oe_ph[t], kSite | 6)) return false;
+            oe_ph[t] ^= 1;
           }
-          mma_commit(bar(S_FULL + t));
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kKeys / 16; ++kk) {  // 16 keys = 8 TMEM columns of P, 2 KB of V
+            mma_ts(tbase + kTmemO + t * 128, tbase + kTmemS + t * 128 + kk * 8,
+                   vdesc + ((kk * 2048) >> 4), kIdescPV, (!first_pv[t] || kk > 0) ? 1u : 0u);
+          }
+          pf_ph[t] ^= 1;
+          first_pv[t] = false;
+          return true;
+        };
+        for (int j = 0; ok && j < it.n_kv; ++j) {
+          const uint32_t k_slot = slot;
+          if (!(ok = wait_one(bar(KV_FULL + k_slot), ph, kSite | 4))) break;
+          if (++slot == kSlots) { slot = 0; ph ^= 1; }
+          const uint32_t nv_slot = slot, nv_ph = ph;
+          if (++slot == kSlots) { slot = 0; ph ^= 1; }
+          if (j > 0) {
+            if (!(ok = wait_one(bar(KV_FULL + v_slot), v_ph, kSite | 4))) break;
+          }
+          tc_fence_after();
+          const uint64_t kdesc = dK + ((sKV + k_slot * kTileBytes) >> 4);
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (j > 0 && !(ok = issue_pv(t))) break;
+            const uint64_t qdesc = dK + ((sQ + t * kTileBytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < kHeadDim / 16; ++kk) {  // 16 columns of d = 32 B of a row
+              const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+              mma_ss(tbase + kTmemS + t * 128, qdesc + off, kdesc + off, kIdescS,
+                     kk > 0 ? 1u : 0u);
+            }
+            mma_commit(bar(S_FULL + t));
+          }
+          if (!ok) break;
+          mma_commit(bar(KV_EMPTY + k_slot));
+          if (j > 0) mma_commit(bar(KV_EMPTY + v_slot));
+          if (j == it.n_kv - 1) mma_commit(bar(Q_EMPTY));
+          v_slot = nv_slot;
+          v_ph = nv_ph;
         }
         if (!ok) break;
-        mma_commit(bar(KV_EMPTY + k_slot));
-        if (j > 0) mma_commit(bar(KV_EMPTY + v_slot));
-        if (j == it.n_kv - 1) mma_commit(bar(Q_EMPTY));
-        v_slot = nv_slot;
-        v_ph = nv_ph;
+        if (!(ok = wait_one(bar(KV_FULL + v_slot), v_ph, kSite | 4))) break;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (!(ok = issue_pv(t))) break;
+          mma_commit(bar(O_FULL + t));
+        }
+        if (!ok) break;
+        mma_commit(bar(KV_EMPTY + v_slot));
+        ++done;
       }
-      if (!ok) break;
-      if (!(ok = wait_bounded(bar(KV_FULL + v_slot), v_ph, abort_flag, p.err, kSite | 4))) break;
-      for (int t = 0; t < 2 && ok; ++t) {
-        if (!(ok = issue_pv(t))) break;
-        mma_commit(bar(O_FULL + t));
+      if (!ok) {  // wait for every MMA already issued before TMEM is released
+        mma_commit(bar(DRAIN));
+        wait_drain(bar(DRAIN), 0, 200000000ull);
       }
-      if (!ok) break;
-      mma_commit(bar(KV_EMPTY + v_slot));
-      ++done;
     }
-    if (!ok) {  // wait for every MMA already issued before TMEM is released
-      mma_commit(bar(DRAIN));
-      wait_drain(bar(DRAIN), 0, 200000000ull);
-    }
-  } else if (warp >= 4) {
+  } else {
     // ------------------------------------------------------------ softmax
-    const int t = (warp - 4) >> 2;                  // query tile of this warpgroup
-    const int wq = warp & 3;                        // TMEM lane quarter
+    const int t = (warp - 4) >> 2;
+    const int wq = warp & 3;
     const uint32_t lane_off = static_cast<uint32_t>(32 * wq) << 16;
     const uint32_t tS = tbase + lane_off + kTmemS + t * 128;
     const uint32_t tO = tbase + lane_off + kTmemO + t * 128;
@@ -318,33 +332,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.causal) limit = min(limit, row + 1 + (p.Nk - p.Nq));
       float m_ref = kNegInf, l = 0.f;
       for (int j = 0; j < it.n_kv; ++j) {
-        ok = __all_sync(0xffffffffu,
-                        wait_bounded(bar(S_FULL + t), sf_ph, abort_flag, p.err, kSite | 7));
+        ok = wait_all(bar(S_FULL + t), sf_ph, kSite | 7);
         if (!ok) break;
         sf_ph ^= 1;
         tc_fence_after();
         uint32_t sr[128];
-        tmem_ld_x128(tS, sr);
         const int k0 = j * kKeys;
-        if (__any_sync(0xffffffffu, k0 + kKeys > limit)) {
+        const bool masked_tile = __any_sync(0xffffffffu, k0 + kKeys > limit);
+        float mx[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
+        if (masked_tile) {
+          tmem_ld_x128(tS, sr);
 #pragma unroll
           for (int c = 0; c < 128; ++c)
             if (k0 + c >= limit) sr[c] = __float_as_uint(kNegInf);
-        }
-        float mx[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
 #pragma unroll
-        for (int c = 0; c < 128; c += 4) {
-          mx[0] = fmaxf(mx[0], __uint_as_float(sr[c]));
-          mx[1] = fmaxf(mx[1], __uint_as_float(sr[c + 1]));
-          mx[2] = fmaxf(mx[2], __uint_as_float(sr[c + 2]));
-          mx[3] = fmaxf(mx[3], __uint_as_float(sr[c + 3]));
+          for (int c = 0; c < 128; c += 8) {
+            mx[0] = max3(mx[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+            mx[1] = max3(mx[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+            mx[2] = max3(mx[2], __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+            mx[3] = max3(mx[3], __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+          }
+        } else {
+          tmem_ld_x64(tS, *reinterpret_cast<uint32_t(*)[64]>(sr));
+          tmem_ld_x64_nowait(tS + 64, sr + 64);
+#pragma unroll
+          for (int c = 0; c < 64; c += 8) {
+            mx[0] = max3(mx[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+            mx[1] = max3(mx[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+            mx[2] = max3(mx[2], __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+            mx[3] = max3(mx[3], __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+          }
+          tmem_wait_ld_dep64(sr + 64);
+#pragma unroll
+          for (int c = 64; c < 128; c += 8) {
+            mx[0] = max3(mx[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+            mx[1] = max3(mx[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+            mx[2] = max3(mx[2], __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+            mx[3] = max3(mx[3], __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+          }
         }
         const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
         const float m_new = fmaxf(m_ref, m_tile);
         float alpha = 1.f;
         bool resc = false;
         if (m_ref == kNegInf) {
-          m_ref = m_new;  // nothing summed yet: l = 0 and O~ = 0
+          m_ref = m_new;
         } else if (m_new > m_ref + kTau) {
           alpha = ex2(m_ref - m_new);
           l *= alpha;
@@ -352,8 +384,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           resc = true;
         }
         if (__any_sync(0xffffffffu, resc)) {
-          // O~ has every earlier P V product in it (the commit that signalled S
-          // also covers the previous P V), and nothing writes it until P is ready
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t orr[32];
@@ -364,26 +394,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         const float nref = (m_ref == kNegInf) ? 0.f : -m_ref;
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t pk[64];
+        // pass 2, rolled over four 32-column chunks (S reloaded from TMEM), each
+        // chunk two-phase: all scale/subtracts, then 32 independent exp2, then
+        // the sums and bf16 packs -- so the MUFU latency is covered
+        float la[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t sc[32], pk[16];
+          float pv[32];
+          tmem_ld_x32(tS + 32 * ch, sc);
+          if (masked_tile) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), sl2, nref));
-          const float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, nref));
-          ls[c & 3] += p0 + p1;
-          __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-          pk[c] = *reinterpret_cast<uint32_t*>(&h2);
+            for (int e = 0; e < 32; ++e)
+              if (k0 + 32 * ch + e >= limit) sc[e] = __float_as_uint(kNegInf);
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            fma2(pv[2 * i], pv[2 * i + 1], __uint_as_float(sc[2 * i]), __uint_as_float(sc[2 * i + 1]),
+                 sl2, sl2, nref, nref);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) pv[e] = ex2(pv[e]);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            add2(la[2 * (i & 1)], la[2 * (i & 1) + 1], pv[2 * i], pv[2 * i + 1]);
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(pv[2 * i], pv[2 * i + 1]);
+            pk[i] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          tmem_st_x16_nowait(tS + 16 * ch, pk);
         }
-        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        tmem_st_x64(tS, pk);
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(P_FULL + t));
+        if (lane == 0) {
+          mbar_arrive(bar(P_FULL + t));
+        }
+        l += (la[0] + la[1]) + (la[2] + la[3]);
       }
       if (!ok) break;
-      // epilogue: O = O~ / l, lse = ln2 * (m + log2 l)
-      ok = __all_sync(0xffffffffu,
-                      wait_bounded(bar(O_FULL + t), of_ph, abort_flag, p.err, kSite | 8));
+      ok = wait_all(bar(O_FULL + t), of_ph, kSite | 8);
       if (!ok) break;
       of_ph ^= 1;
       tc_fence_after();
