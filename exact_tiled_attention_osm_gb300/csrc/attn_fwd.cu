@@ -36,6 +36,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "internal.h"
@@ -51,6 +52,7 @@ constexpr int kHeadDim = 128;
 constexpr int kRows = 128;   // query rows per tile (MMA M)
 constexpr int kKeys = 128;   // keys per K/V tile (MMA N of QK^T, K of PV)
 constexpr int kSlots = 4;    // K/V ring slots, one 32 KB tile each
+constexpr int kItemSlots = 4;  // depth of the CTA's queue of work-item numbers
 constexpr uint32_t kTileBytes = kRows * kHeadDim * 2;  // 32768
 constexpr uint32_t kBoxBytes = 128 * 64 * 2;           // one TMA box: 64 columns x 128 rows
 constexpr int kThreads = 384;
@@ -72,11 +74,16 @@ enum Bar : uint32_t {
   O_FULL = P_FULL + 2,       // [2]
   O_EMPTY = O_FULL + 2,      // [2]
   DRAIN = O_EMPTY + 2,
-  NUM_BARS
+  ITEM_FULL = DRAIN + 1,     // [kItemSlots]
+  ITEM_EMPTY = ITEM_FULL + kItemSlots,  // [kItemSlots]
+  NUM_BARS = ITEM_EMPTY + kItemSlots
 };
 constexpr uint32_t kSmemTmemSlot = kSmemBar + 8 * NUM_BARS;
 constexpr uint32_t kSmemAbort = kSmemTmemSlot + 4;
-constexpr uint32_t kSmemBytes = kSmemAbort + 4 + 1024;  // + alignment slack
+constexpr uint32_t kSmemItems = kSmemAbort + 4;  // int[kItemSlots]: the CTA's item queue
+constexpr uint32_t kSmemBytes = kSmemItems + 4 * kItemSlots + 1024;  // + alignment slack
+// readers of the item queue: the MMA thread and the eight softmax warps
+constexpr uint32_t kItemReaders = 1 + 8;
 
 // TMEM columns
 constexpr uint32_t kTmemS = 0;
@@ -98,6 +105,7 @@ struct Params {
   __nv_bfloat16* o;
   float* lse;
   unsigned int* err;
+  unsigned int* next_item;  // work-item counter, zero at launch
 };
 
 struct Item {
@@ -124,8 +132,11 @@ __device__ __forceinline__ Item item_info(const Params& p, int item) {
 }
 
 __device__ unsigned int g_err_word;
-
-// ---- experiment switches (defaults = committed design) ----
+// Work-item counters.  Each launch takes the next entry (round robin) and
+// zeroes it on its own stream first, so launches on different streams only
+// share a counter when more than kCounters of them are in flight at once.
+constexpr int kCounters = 1024;
+__device__ unsigned int g_item_counter[kCounters];
 
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -137,6 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = sbase + kSmemQ, sKV = sbase + kSmemKV;
   auto bar = [&](uint32_t i) { return sbase + kSmemBar + 8 * i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemAbort);
+  volatile int* item_q = reinterpret_cast<volatile int*>(smem + kSmemItems);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSmemTmemSlot);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -156,6 +168,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(KV_EMPTY + s), 1);
     }
     mbar_init(bar(DRAIN), 1);
+    for (int s = 0; s < kItemSlots; ++s) {
+      mbar_init(bar(ITEM_FULL + s), 1);
+      mbar_init(bar(ITEM_EMPTY + s), kItemReaders);
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -167,13 +183,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  // a wait of a group of lanes: every lane polls; with a whole warp the lanes agree
   // bounded waits: by one thread, or by a whole warp that then agrees on the outcome
   auto wait_one = [&](uint32_t b, uint32_t parity, unsigned site) -> bool {
     return wait_bounded(b, parity, abort_flag, p.err, site);
   };
   auto wait_all = [&](uint32_t b, uint32_t parity, unsigned site) -> bool {
     return __all_sync(0xffffffffu, wait_bounded(b, parity, abort_flag, p.err, site));
+  };
+  // Work items are handed out dynamically: the producer thread takes the next
+  // item number from a global counter and passes it to the other roles through
+  // a small queue in shared memory, so every role of the CTA walks the same
+  // item sequence.  -1 ends the sequence.
+  uint32_t iq_slot = 0, iq_ph = 0;
+  auto iq_advance = [&]() {
+    if (++iq_slot == kItemSlots) { iq_slot = 0; iq_ph ^= 1; }
   };
 
   if (warp < 4) {
@@ -187,37 +210,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       int q_fill = -1;
       int loaded = 0;
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x) {
+      auto publish = [&](int item) -> bool {
+        if (!wait_one(bar(ITEM_EMPTY + iq_slot), iq_ph ^ 1, kSite | 9)) return false;
+        item_q[iq_slot] = item;
+        mbar_arrive(bar(ITEM_FULL + iq_slot));
+        iq_advance();
+        return true;
+      };
+      // the first item of every CTA is its own index (grid <= items); the
+      // rest come from the counter, one item ahead of the one being loaded
+      int item = blockIdx.x;
+      ok = publish(item);
+      while (ok && item >= 0) {
         const Item it = item_info(p, item);
-        if (it.n_kv == 0) continue;
-        if (loaded > 0) {
-          if (!(ok = wait_one(bar(Q_EMPTY), qe_ph, kSite | 1))) break;
-          qe_ph ^= 1;
-        }
-        for (int t = 0; t < 2; ++t) {
-          mbar_arrive_expect_tx(bar(Q_FULL + t), kTileBytes);
-          for (int c = 0; c < 2; ++c)
-            tma_load_3d(sQ + t * kTileBytes + c * kBoxBytes, &tm_q, bar(Q_FULL + t), c * 64,
-                        it.q0 + t * kRows, it.bh);
-        }
-        q_fill = loaded & 1;
-        ++loaded;
-        for (int j = 0; ok && j < it.n_kv; ++j) {
-          for (int kv = 0; kv < 2; ++kv) {
-            if (!(ok = wait_one(bar(KV_EMPTY + slot), ph ^ 1, kSite | 2))) break;
-            mbar_arrive_expect_tx(bar(KV_FULL + slot), kTileBytes);
-            const CUtensorMap* tm = kv ? &tm_v : &tm_k;
-            for (int c = 0; c < 2; ++c)
-              tma_load_3d(sKV + slot * kTileBytes + c * kBoxBytes, tm, bar(KV_FULL + slot),
-                          c * 64, j * kKeys, it.bh);
-            fill_mask |= 1u << slot;
-            fill_ph = (fill_ph & ~(1u << slot)) | (ph << slot);
-            if (++slot == kSlots) {
-              slot = 0;
-              ph ^= 1;
-            }
+        bool published = false;
+        unsigned int ticket = 0;
+        auto publish_next = [&]() -> bool {
+          published = true;
+          const int64_t nx = static_cast<int64_t>(gridDim.x) + ticket;
+          item = nx < p.num_items ? static_cast<int>(nx) : -1;
+          return publish(item);
+        };
+        if (it.n_kv > 0) {
+          if (loaded > 0) {
+            if (!(ok = wait_one(bar(Q_EMPTY), qe_ph, kSite | 1))) break;
+            qe_ph ^= 1;
           }
+          for (int t = 0; t < 2; ++t) {
+            mbar_arrive_expect_tx(bar(Q_FULL + t), kTileBytes);
+            for (int c = 0; c < 2; ++c)
+              tma_load_3d(sQ + t * kTileBytes + c * kBoxBytes, &tm_q, bar(Q_FULL + t), c * 64,
+                          it.q0 + t * kRows, it.bh);
+          }
+          q_fill = loaded & 1;
+          ++loaded;
+          // the counter's reply is first needed after this item's first K/V copies
+          ticket = atomicAdd(p.next_item, 1u);
+          for (int j = 0; ok && j < it.n_kv; ++j) {
+            for (int kv = 0; kv < 2; ++kv) {
+              if (!(ok = wait_one(bar(KV_EMPTY + slot), ph ^ 1, kSite | 2))) break;
+              mbar_arrive_expect_tx(bar(KV_FULL + slot), kTileBytes);
+              const CUtensorMap* tm = kv ? &tm_v : &tm_k;
+              for (int c = 0; c < 2; ++c)
+                tma_load_3d(sKV + slot * kTileBytes + c * kBoxBytes, tm, bar(KV_FULL + slot),
+                            c * 64, j * kKeys, it.bh);
+              fill_mask |= 1u << slot;
+              fill_ph = (fill_ph & ~(1u << slot)) | (ph << slot);
+              if (++slot == kSlots) {
+                slot = 0;
+                ph ^= 1;
+              }
+            }
+            if (ok && !published) ok = publish_next();
+          }
+        } else {
+          ticket = atomicAdd(p.next_item, 1u);
         }
+        if (ok && !published) ok = publish_next();
       }
       if (!ok) {  // let every copy this thread started land before the CTA exits
         for (int s = 0; s < kSlots; ++s)
@@ -233,7 +282,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       const uint64_t dK = sdesc_sw128(0, 16, 1024);     // K-major template (address added)
       const uint64_t dV = sdesc_sw128(0, 16384, 1024);  // MN-major template
-      for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x) {
+      while (ok) {
+        if (!(ok = wait_one(bar(ITEM_FULL + iq_slot), iq_ph, kSite | 10))) break;
+        const int item = item_q[iq_slot];
+        mbar_arrive(bar(ITEM_EMPTY + iq_slot));
+        iq_advance();
+        if (item < 0) break;
         const Item it = item_info(p, item);
         if (it.n_kv == 0) continue;
         for (int t = 0; t < 2 && ok; ++t) ok = wait_one(bar(Q_FULL + t), qf_ph, kSite | 3);
@@ -314,7 +368,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     uint32_t sf_ph = 0, of_ph = 0;
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x) {
+    while (ok) {
+      if (!(ok = wait_all(bar(ITEM_FULL + iq_slot), iq_ph, kSite | 11))) break;
+      const int item = item_q[iq_slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(ITEM_EMPTY + iq_slot));
+      iq_advance();
+      if (item < 0) break;
       const Item it = item_info(p, item);
       const int row = it.q0 + t * kRows + 32 * wq + lane;
       const bool row_ok = row < p.Nq;
@@ -521,6 +581,13 @@ cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o
   cudaError_t e = cudaGetSymbolAddress(&errp, g_err_word);
   if (e != cudaSuccess) return e;
   p.err = static_cast<unsigned int*>(errp);
+  void* ctrp = nullptr;
+  e = cudaGetSymbolAddress(&ctrp, g_item_counter);
+  if (e != cudaSuccess) return e;
+  static std::atomic<unsigned int> next_counter{0};
+  p.next_item = static_cast<unsigned int*>(ctrp) + next_counter.fetch_add(1) % kCounters;
+  e = cudaMemsetAsync(p.next_item, 0, sizeof(unsigned int), s);
+  if (e != cudaSuccess) return e;
   // the shared-memory opt-in is per function and per device
   static unsigned long long attr_done = 0;
   int dev = 0;
