@@ -321,7 +321,8 @@ def reduce_max(times: dict, world: int, device) -> dict:
 def profile_case(spec: str, iters: int):
     """Run one operation `iters` times on a given shape (for ncu captures).
 
-    spec: "attn:B,H,N[,causal]" | "softmax:rows,cols" | "decode:B,H,Nk[,splits]".
+    spec: "attn:B,H,N[,causal]" | "softmax:rows,cols" | "decode:B,H,Nk[,splits]"
+          | "append:B,H,Nk,n_new[,splits]".
     Inputs come from the same generators as the full workloads.
     """
     import exact_tiled_attention_osm_gb300 as osm
@@ -352,6 +353,22 @@ def profile_case(spec: str, iters: int):
         run = lambda: osm.attn_decode_splitkv(dc.q, dc.k, dc.v, dc.scale, dc.key_len, S,
                                               workspace=ws)
         work, unit = decode_bytes(B, H, 128, dc.key_len.cpu().numpy()), "GB/s"
+    elif op == "append":
+        # extend running summaries by the last n_new keys of a B x H x Nk cache
+        B, H, Nk, n_new = (int(x) for x in parts[:4])
+        S = int(parts[4]) if len(parts) > 4 else 16
+        dc = W.decode(5, B=B, H=H, Nk=Nk, len_range=(Nk, Nk), num_splits=S, device="cuda")
+        ws = torch.empty(osm.decode_append_workspace_bytes(B, H, 128, S), dtype=torch.uint8,
+                         device=dev)
+        state = osm.decode_state(B, H, 128, dev)
+        ks = torch.full((B,), Nk - n_new, dtype=torch.int32, device=dev)
+        osm.attn_decode_append(dc.q, dc.k, dc.v, state, None, ks, dc.scale, S, workspace=ws)
+        run = lambda: osm.attn_decode_append(dc.q, dc.k, dc.v, state, ks, None, dc.scale, S,
+                                             workspace=ws)
+        # new K/V rows + q + o (bf16) + lse + the state read and written (fp32)
+        work = (B * H * n_new * 128 * 2 * 2 + B * H * 128 * 2 * 2 + B * H * 4
+                + 2 * B * H * (128 + 2) * 4)
+        unit = "GB/s"
     else:
         raise SystemExit(f"unknown op {op}")
     run()

@@ -38,6 +38,9 @@ SIGNATURES = {
     "osm_attn_decode_splitkv_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "osm_attn_decode_splitkv": (_I, [_I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _I, _P, _SZ, _P]),
     "osm_attn_decode_splitkv_noalloc": (_I, [_I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _I, _P]),
+    "osm_attn_decode_append_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "osm_attn_decode_append": (_I, [_I, _P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P,
+                                    _P, _I, _P, _SZ, _P]),
     "osm_lse_merge": (_I, [_P, _P, _I, _I64, _I, _I, _P, _P, _P]),
     "osm_status_string": (ctypes.c_char_p, [_I]),
     "osm_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint32)]),
@@ -185,6 +188,66 @@ def attn_decode_splitkv(q, k, v, scale=None, key_len=None, num_splits=16, worksp
                                            float(scale), kl, int(num_splits),
                                            workspace.data_ptr(), workspace.numel(), _stream(q)),
                "osm_attn_decode_splitkv")
+    return o, lse_t
+
+
+def decode_append_workspace_bytes(B: int, H: int, d: int, num_splits: int) -> int:
+    return int(load_library().osm_attn_decode_append_workspace_bytes(B, H, d, num_splits))
+
+
+def decode_state(B: int, H: int, d: int, device) -> tuple:
+    """The empty running summary (m = -inf, l = 0, o~ = 0) for attn_decode_append."""
+    return (torch.full((B, H), -math.inf, dtype=torch.float32, device=device),
+            torch.zeros((B, H), dtype=torch.float32, device=device),
+            torch.zeros((B, H, d), dtype=torch.float32, device=device))
+
+
+def attn_decode_append(q, k, v, state, key_start=None, key_end=None, scale=None,
+                       num_splits=16, workspace=None, out=None, lse=None):
+    """Extend each query's running summary by the keys [key_start[b], key_end[b]).
+
+    q [B,H,1,d]; k, v [B,H,Nk,d] (bf16 or fp32, same dtype); state = (m [B,H],
+    l [B,H], o~ [B,H,d]) fp32 CUDA tensors, updated in place.  Returns (o, lse),
+    the attention output over every key merged into the state so far.
+    """
+    dt = {torch.bfloat16: OSM_BF16, torch.float32: OSM_F32}.get(q.dtype)
+    if dt is None:
+        raise ValueError("decode supports bf16 and fp32")
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype, q.device)
+    B, H, one, d = q.shape
+    if one != 1 or k.dim() != 4 or v.shape != k.shape or k.shape[0] != B or k.shape[1] != H \
+            or k.shape[3] != d:
+        raise ValueError("q must be [B,H,1,d] and k, v [B,H,Nk,d]")
+    Nk = k.shape[2]
+    sm, sl, so = state
+    for t, n, shp in ((sm, "state m", (B, H)), (sl, "state l", (B, H)), (so, "state o", (B, H, d))):
+        _need(t, n, torch.float32, q.device)
+        if tuple(t.shape) != shp:
+            raise ValueError(f"{n} must have shape {shp}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = decode_append_workspace_bytes(B, H, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _need(workspace, "workspace", torch.uint8, q.device)
+    o = torch.empty_like(q) if out is None else out
+    lse_t = torch.empty((B, H), dtype=torch.float32, device=q.device) if lse is None else lse
+    ptrs = []
+    for t, n in ((key_start, "key_start"), (key_end, "key_end")):
+        if t is None:
+            ptrs.append(0)
+        else:
+            _need(t, n, torch.int32, q.device)
+            ptrs.append(t.data_ptr())
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        _check(lib.osm_attn_decode_append(dt, q.data_ptr(), k.data_ptr(), v.data_ptr(), B, H, Nk,
+                                          d, float(scale), ptrs[0], ptrs[1], sm.data_ptr(),
+                                          sl.data_ptr(), so.data_ptr(), o.data_ptr(),
+                                          lse_t.data_ptr(), int(num_splits),
+                                          workspace.data_ptr(), workspace.numel(), _stream(q)),
+               "osm_attn_decode_append")
     return o, lse_t
 
 

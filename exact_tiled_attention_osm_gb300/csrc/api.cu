@@ -19,7 +19,7 @@ inline osm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? OSM_OK : 
 
 extern "C" {
 
-int osm_abi_version(void) { return 100; }
+int osm_abi_version(void) { return 101; }
 
 const char* osm_status_string(osm_status st) {
   switch (st) {
@@ -114,6 +114,40 @@ osm_status osm_attn_decode_splitkv_noalloc(osm_dtype dt, const void* q, const vo
   return from_cuda(osm::launch_decode_splitkv_noalloc(dt, q, k, v, o, lse, B, H, Nk, d, scale,
                                                       key_len, num_splits,
                                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t osm_attn_decode_append_workspace_bytes(int B, int H, int d, int num_splits) {
+  if (B < 0 || H < 0 || (d != 64 && d != 128) || num_splits < 1 || num_splits > 256) return 0;
+  return osm::decode_append_workspace_bytes(B, H, d, num_splits);
+}
+
+osm_status osm_attn_decode_append(osm_dtype dt, const void* q, const void* k, const void* v,
+                                  int B, int H, int Nk, int d, float scale,
+                                  const int32_t* key_start, const int32_t* key_end,
+                                  float* state_m, float* state_l, float* state_o, void* o,
+                                  float* lse, int num_splits, void* workspace,
+                                  size_t workspace_bytes, osm_stream_t stream) {
+  if (dt != OSM_F32 && dt != OSM_BF16) return OSM_ERR_INVALID_VALUE;
+  if (B < 0 || H < 0 || Nk < 0) return OSM_ERR_INVALID_VALUE;
+  if (d != 64 && d != 128) return (d > 0) ? OSM_ERR_UNSUPPORTED : OSM_ERR_INVALID_VALUE;
+  if (num_splits < 1 || num_splits > 256) return OSM_ERR_INVALID_VALUE;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return OSM_ERR_INVALID_VALUE;
+  if (static_cast<int64_t>(B) * H == 0) return OSM_OK;
+  if (B > 65535 || H > 65535) return OSM_ERR_UNSUPPORTED;
+  if (!q || !state_m || !state_l || !state_o || !workspace || (Nk > 0 && (!k || !v)))
+    return OSM_ERR_INVALID_VALUE;
+  if (!aligned16(q) || !aligned4(state_m) || !aligned4(state_l) || !aligned4(state_o))
+    return OSM_ERR_INVALID_VALUE;
+  if ((o && !aligned4(o)) || (lse && !aligned4(lse))) return OSM_ERR_INVALID_VALUE;
+  if (Nk > 0 && (!aligned16(k) || !aligned16(v))) return OSM_ERR_INVALID_VALUE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return OSM_ERR_INVALID_VALUE;
+  if ((key_start && !aligned4(key_start)) || (key_end && !aligned4(key_end)))
+    return OSM_ERR_INVALID_VALUE;
+  if (workspace_bytes < osm::decode_append_workspace_bytes(B, H, d, num_splits))
+    return OSM_ERR_INVALID_VALUE;
+  return from_cuda(osm::launch_decode_append(dt, q, k, v, B, H, Nk, d, scale, key_start, key_end,
+                                             state_m, state_l, state_o, o, lse, num_splits,
+                                             workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 osm_status osm_lse_merge(const float* o_parts, const float* lse_parts, int S, int64_t rows, int d,

@@ -78,12 +78,27 @@ struct Workspace {
   float* l;
   float* o;
 };
+// Running summaries extended in place by the append form of the split kernel.
+struct AppendState {
+  float* m;               // [rows] natural-log units
+  float* l;               // [rows]
+  float* o;               // [rows][D] unnormalised
+  void* out;              // [rows][D] normalised output (bf16 or fp32), or null
+  float* lse;             // [rows], or null
+  int out_bf16;
+  unsigned int* tickets;  // [rows], zero at launch
+};
 __host__ __device__ inline size_t ws_section(int64_t n) { return ((n * 4 + 255) / 256) * 256; }
 
-template <typename T, int D>
+// APPEND: the keys are [key_start[b], key_len[b]) and the CTA that finishes a
+// row last (a ticket counter, no waiting) merges the row's split summaries
+// into the stored running summary: state <- state (+) split_0 (+) ... (+)
+// split_{S-1}, then writes the normalised output.
+template <typename T, int D, bool APPEND>
 __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
-    const int32_t* __restrict__ key_len, int H, int Nk, int S, float scale_log2, Workspace ws) {
+    const int32_t* __restrict__ key_len, int H, int Nk, int S, float scale_log2, Workspace ws,
+    const int32_t* __restrict__ key_start, AppendState st) {
   using C = Cfg<T, D>;
   constexpr int EPL = C::EPL, LPK = C::LPK, KPP = C::KPP, R = C::R, BLOCK = C::BLOCK;
   __shared__ float sm_m[kWarps], sm_l[kWarps];
@@ -96,9 +111,12 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(
   const int64_t row = static_cast<int64_t>(b) * H + h;
   int L = key_len ? key_len[b] : Nk;
   L = L < 0 ? 0 : (L > Nk ? Nk : L);
-  const int chunk = (L + S - 1) / S;
-  const int k_begin = min(L, s * chunk);
-  const int k_end = min(L, k_begin + chunk);
+  int K0 = 0;
+  if (APPEND && key_start) K0 = min(max(key_start[b], 0), L);
+  const int n = L - K0;
+  const int chunk = (n + S - 1) / S;
+  const int k_begin = K0 + min(n, s * chunk);
+  const int k_end = K0 + min(n, s * chunk + chunk);
 
   // query slice, pre-multiplied by scale*log2(e) so scores come out in base-2 units
   float qf[EPL];
@@ -202,6 +220,51 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(
     ws.m[p] = (M == kNegInf) ? kNegInf : M * kLn2;  // natural-log units
     ws.l[p] = Lt;
   }
+  if constexpr (APPEND) {
+    __shared__ int sm_last;
+    __threadfence();  // this split's summary is visible before its ticket is
+    __syncthreads();
+    if (threadIdx.x == 0) sm_last = atomicAdd(st.tickets + row, 1u) == static_cast<unsigned>(S - 1);
+    __syncthreads();
+    if (!sm_last) return;
+    __threadfence();
+    const int64_t R = static_cast<int64_t>(gridDim.y) * gridDim.z;
+    // merge in the fixed order: stored summary, then splits 0 .. S-1
+    const float m0 = st.m[row];
+    float Mg = m0;
+    for (int t = 0; t < S; ++t) Mg = fmaxf(Mg, __ldcg(ws.m + t * R + row));
+    float lg = 0.f, og = 0.f;
+    const int c = threadIdx.x;
+    if (Mg != kNegInf) {
+      if (m0 != kNegInf) {
+        const float w = ptx::ex2((m0 - Mg) * kLog2e);
+        lg = st.l[row] * w;
+        if (c < D) og = st.o[row * D + c] * w;
+      }
+      for (int t = 0; t < S; ++t) {
+        const float mt = __ldcg(ws.m + t * R + row);
+        if (mt == kNegInf) continue;
+        const float w = ptx::ex2((mt - Mg) * kLog2e);
+        lg = fmaf(__ldcg(ws.l + t * R + row), w, lg);
+        if (c < D) og = fmaf(__ldcg(ws.o + (t * R + row) * D + c), w, og);
+      }
+    }
+    if (c < D) {
+      st.o[row * D + c] = og;
+      if (st.out) {
+        const float val = lg > 0.f ? og / lg : 0.f;
+        if (st.out_bf16)
+          static_cast<__nv_bfloat16*>(st.out)[row * D + c] = __float2bfloat16_rn(val);
+        else
+          static_cast<float*>(st.out)[row * D + c] = val;
+      }
+    }
+    if (c == 0) {
+      st.m[row] = Mg;
+      st.l[row] = lg;
+      if (st.lse) st.lse[row] = lg > 0.f ? Mg + logf(lg) : kNegInf;
+    }
+  }
 }
 
 template <typename T>
@@ -293,23 +356,23 @@ cudaError_t launch_decode_splitkv(osm_dtype dt, const void* q, const void* k, co
   if (dt == OSM_BF16) {
     using T = __nv_bfloat16;
     if (d == 128)
-      decode_split_kernel<T, 128><<<grid, block, 0, s>>>(
+      decode_split_kernel<T, 128, false><<<grid, block, 0, s>>>(
           static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), key_len,
-          H, Nk, S, sl2, ws);
+          H, Nk, S, sl2, ws, nullptr, AppendState{});
     else
-      decode_split_kernel<T, 64><<<grid, block, 0, s>>>(
+      decode_split_kernel<T, 64, false><<<grid, block, 0, s>>>(
           static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), key_len,
-          H, Nk, S, sl2, ws);
+          H, Nk, S, sl2, ws, nullptr, AppendState{});
   } else {
     using T = float;
     if (d == 128)
-      decode_split_kernel<T, 128><<<grid, block, 0, s>>>(
+      decode_split_kernel<T, 128, false><<<grid, block, 0, s>>>(
           static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), key_len,
-          H, Nk, S, sl2, ws);
+          H, Nk, S, sl2, ws, nullptr, AppendState{});
     else
-      decode_split_kernel<T, 64><<<grid, block, 0, s>>>(
+      decode_split_kernel<T, 64, false><<<grid, block, 0, s>>>(
           static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), key_len,
-          H, Nk, S, sl2, ws);
+          H, Nk, S, sl2, ws, nullptr, AppendState{});
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -355,6 +418,48 @@ cudaError_t launch_decode_splitkv_noalloc(osm_dtype dt, const void* q, const voi
   cudaError_t e = noalloc_scratch_address(&scratch);
   if (e != cudaSuccess) return e;
   return launch_decode_splitkv(dt, q, k, v, o, lse, B, H, Nk, d, scale, key_len, S, scratch, s);
+}
+
+size_t decode_append_workspace_bytes(int B, int H, int d, int S) {
+  return decode_workspace_bytes(B, H, d, S) + ws_section(static_cast<int64_t>(B) * H);
+}
+
+cudaError_t launch_decode_append(osm_dtype dt, const void* q, const void* k, const void* v,
+                                 int B, int H, int Nk, int d, float scale,
+                                 const int32_t* key_start, const int32_t* key_end, float* state_m,
+                                 float* state_l, float* state_o, void* o, float* lse, int S,
+                                 void* ws_ptr, cudaStream_t s) {
+  const int64_t rows = static_cast<int64_t>(B) * H;
+  Workspace ws = carve(ws_ptr, rows * S, d);
+  unsigned int* tickets = reinterpret_cast<unsigned int*>(
+      static_cast<char*>(ws_ptr) + decode_workspace_bytes(B, H, d, S));
+  cudaError_t e = cudaMemsetAsync(tickets, 0, static_cast<size_t>(rows) * 4, s);
+  if (e != cudaSuccess) return e;
+  const AppendState st{state_m, state_l, state_o, o, lse, dt == OSM_BF16 ? 1 : 0, tickets};
+  const float sl2 = scale * kLog2e;
+  const dim3 grid(S, H, B), block(kWarps * 32);
+  if (dt == OSM_BF16) {
+    using T = __nv_bfloat16;
+    const T *tq = static_cast<const T*>(q), *tk = static_cast<const T*>(k),
+            *tv = static_cast<const T*>(v);
+    if (d == 128)
+      decode_split_kernel<T, 128, true>
+          <<<grid, block, 0, s>>>(tq, tk, tv, key_end, H, Nk, S, sl2, ws, key_start, st);
+    else
+      decode_split_kernel<T, 64, true>
+          <<<grid, block, 0, s>>>(tq, tk, tv, key_end, H, Nk, S, sl2, ws, key_start, st);
+  } else {
+    using T = float;
+    const T *tq = static_cast<const T*>(q), *tk = static_cast<const T*>(k),
+            *tv = static_cast<const T*>(v);
+    if (d == 128)
+      decode_split_kernel<T, 128, true>
+          <<<grid, block, 0, s>>>(tq, tk, tv, key_end, H, Nk, S, sl2, ws, key_start, st);
+    else
+      decode_split_kernel<T, 64, true>
+          <<<grid, block, 0, s>>>(tq, tk, tv, key_end, H, Nk, S, sl2, ws, key_start, st);
+  }
+  return cudaGetLastError();
 }
 
 cudaError_t launch_lse_merge(const float* o_parts, const float* lse_parts, int S, int64_t rows,

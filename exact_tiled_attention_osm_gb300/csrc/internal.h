@@ -30,6 +30,13 @@ cudaError_t launch_decode_splitkv_noalloc(osm_dtype dt, const void* q, const voi
                                           const void* v, void* o, float* lse, int B, int H,
                                           int Nk, int d, float scale, const int32_t* key_len,
                                           int S, cudaStream_t s);
+// extend stored running summaries by the keys [key_start[b], key_end[b])
+size_t decode_append_workspace_bytes(int B, int H, int d, int S);
+cudaError_t launch_decode_append(osm_dtype dt, const void* q, const void* k, const void* v,
+                                 int B, int H, int Nk, int d, float scale,
+                                 const int32_t* key_start, const int32_t* key_end, float* state_m,
+                                 float* state_l, float* state_o, void* o, float* lse, int S,
+                                 void* ws, cudaStream_t s);
 cudaError_t launch_lse_merge(const float* o_parts, const float* lse_parts, int S, int64_t rows,
                              int d, osm_dtype out_dt, void* o, float* lse, cudaStream_t s);
 

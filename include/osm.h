@@ -200,6 +200,53 @@ osm_status osm_attn_decode_splitkv_noalloc(osm_dtype dt, const void *q, const vo
                                            int Nk, int d, float scale, const int32_t *key_len,
                                            int num_splits, osm_stream_t stream);
 
+/*
+ * osm_attn_decode_append — extend each query's stored running summary by
+ * newly appended keys, and return the attention output over every key seen.
+ *
+ * Defines: for each (b, h) with query q = q[b, h, 0], the caller keeps the
+ * summary (m, l, o~) of the keys already seen: m = max s_j, l = sum_j
+ * exp(s_j - m), o~ = sum_j exp(s_j - m) v_j over those keys ([P3] "Merging
+ * partial results"; the empty set's summary is the identity (-inf, 0, 0)).
+ * Appending keys is one more step of the recurrence ([P1] "How does this
+ * connect to KV-cache decoding?"): the call forms the summary of the keys
+ * [key_start[b], key_end[b]) of k, v and merges it into the stored one
+ * ([P3] "Merging partial results", property 3: one step is a merge), so after
+ * the call the state is the summary of old keys and new keys together, and
+ *   o[b, h] = o~ / l,   lse[b, h] = m + log l   (0 and -inf while l = 0).
+ * The result equals attention over the union up to rounding, whatever the
+ * number and sizes of the appends.
+ *
+ * Work: the new keys are split as in osm_attn_decode_splitkv (range
+ * [key_start, key_end) divided into num_splits equal chunks); the thread block
+ * that finishes a row last (counted with an atomic ticket, no device wait)
+ * merges the row's split summaries into the state, in the fixed order
+ * state, split 0 .. num_splits - 1.  One memset (the tickets) and one kernel
+ * on `stream`.
+ *
+ *   dt         OSM_BF16 (q, k, v, o bf16) or OSM_F32 (all fp32).
+ *   q          [B, H, 1, d];  k, v [B, H, Nk, d] (e.g. a KV cache of capacity Nk).
+ *   key_start  device int32[B] or NULL (= 0); key_end device int32[B] or NULL
+ *              (= Nk).  key_end is clamped to [0, Nk] and key_start to
+ *              [0, key_end]; an empty range leaves the state unchanged.
+ *   state_m    [B, H] fp32, natural-log units of the scaled scores (-inf: no key yet).
+ *   state_l    [B, H] fp32.   state_o [B, H, d] fp32 (unnormalised).
+ *              Read and rewritten in place; start from (-inf, 0, 0).
+ *   o          [B, H, 1, d] in dt, or NULL;  lse [B, H] fp32, or NULL.
+ *   d 64 or 128;  num_splits 1..256;  q, k, v 16-byte aligned.
+ *   workspace  >= osm_attn_decode_append_workspace_bytes(B, H, d, num_splits)
+ *              bytes, 256-byte aligned: the split summaries (the layout of
+ *              osm_attn_decode_splitkv's workspace) followed by B*H tickets.
+ * Launches on one stream must not share a workspace or a state concurrently.
+ */
+size_t osm_attn_decode_append_workspace_bytes(int B, int H, int d, int num_splits);
+osm_status osm_attn_decode_append(osm_dtype dt, const void *q, const void *k, const void *v,
+                                  int B, int H, int Nk, int d, float scale,
+                                  const int32_t *key_start, const int32_t *key_end,
+                                  float *state_m, float *state_l, float *state_o, void *o,
+                                  float *lse, int num_splits, void *workspace,
+                                  size_t workspace_bytes, osm_stream_t stream);
+
 /* Text for a status code (static storage; never NULL). */
 const char *osm_status_string(osm_status status);
 

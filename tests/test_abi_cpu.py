@@ -51,7 +51,7 @@ def test_status_strings_and_version(lib):
         s = osm.status_string(st)
         assert s.startswith("OSM_")
     assert "unknown" in osm.status_string(99)
-    assert lib.osm_abi_version() == 100
+    assert lib.osm_abi_version() == 101
 
 
 def test_workspace_bytes_formula(lib):
@@ -133,6 +133,38 @@ def test_decode_and_merge_validation(lib):
     assert m(FAKE, FAKE, 2, 4, 100, osm.OSM_F32, FAKE, FAKE, None) == osm.OSM_ERR_UNSUPPORTED
     assert m(FAKE, FAKE, 2, 4, 128, 5, FAKE, FAKE, None) == osm.OSM_ERR_INVALID_VALUE
     assert m(FAKE, FAKE, 2, 0, 128, osm.OSM_F32, FAKE, FAKE, None) == osm.OSM_OK
+
+
+def test_append_validation(lib):
+    f = lib.osm_attn_decode_append
+    need = osm.decode_append_workspace_bytes(2, 2, 128, 4)
+    # partial summaries as for split decode, then one ticket per (b, h) row
+    assert need == osm.decode_workspace_bytes(2, 2, 128, 4) + 256
+    assert osm.decode_append_workspace_bytes(2, 2, 96, 4) == 0
+    names = ["dt", "q", "k", "v", "B", "H", "Nk", "d", "scale", "ks", "ke", "m", "l", "o~",
+             "o", "lse", "S", "ws", "wsb", "s"]
+    base = [osm.OSM_BF16, FAKE, FAKE, FAKE, 2, 2, 1000, 128, 0.088, None, None, FAKE, FAKE, FAKE,
+            FAKE, FAKE, 4, FAKE, need, None]
+
+    def call(**kw):
+        a = list(base)
+        for key, val in kw.items():
+            a[names.index(key)] = val
+        return f(*a)
+
+    assert call(dt=7) == osm.OSM_ERR_INVALID_VALUE
+    assert call(q=None) == osm.OSM_ERR_INVALID_VALUE
+    assert call(m=None) == osm.OSM_ERR_INVALID_VALUE       # the state is required
+    assert call(l=None) == osm.OSM_ERR_INVALID_VALUE
+    assert call(**{"o~": None}) == osm.OSM_ERR_INVALID_VALUE
+    assert call(m=FAKE + 2) == osm.OSM_ERR_INVALID_VALUE   # misaligned state
+    assert call(ks=FAKE + 1) == osm.OSM_ERR_INVALID_VALUE
+    assert call(d=96) == osm.OSM_ERR_UNSUPPORTED
+    assert call(S=0) == osm.OSM_ERR_INVALID_VALUE
+    assert call(ws=FAKE + 16) == osm.OSM_ERR_INVALID_VALUE
+    assert call(wsb=need - 1) == osm.OSM_ERR_INVALID_VALUE
+    assert call(scale=float("nan")) == osm.OSM_ERR_INVALID_VALUE
+    assert call(B=0, q=None, m=None, l=None, ws=None) == osm.OSM_OK   # empty: no-op
 
 
 def test_binding_refuses_cpu_tensors():
