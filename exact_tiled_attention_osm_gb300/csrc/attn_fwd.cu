@@ -57,6 +57,9 @@ constexpr uint32_t kTileBytes = kRows * kHeadDim * 2;  // 32768
 constexpr uint32_t kBoxBytes = 128 * 64 * 2;           // one TMA box: 64 columns x 128 rows
 constexpr int kThreads = 384;
 constexpr float kTau = 8.0f;
+// Tiles after a row's first skip the max: a 32-term chunk whose sum stays at
+// or below kSumLimit has no term above it (all terms are >= 0), so P <= 2^16.
+constexpr float kSumLimit = 65536.0f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNegInf = -__builtin_huge_valf();
 
@@ -396,64 +399,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         sf_ph ^= 1;
         tc_fence_after();
-        uint32_t sr[128];
         const int k0 = j * kKeys;
         const bool masked_tile = __any_sync(0xffffffffu, k0 + kKeys > limit);
-        float mx[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
-        if (masked_tile) {
-          tmem_ld_x128(tS, sr);
+        // A row's first tile (no reference yet) takes the tile max first.  Later
+        // tiles go straight to the exponentials against the current reference;
+        // a chunk whose sum shows a term above kSumLimit raises the reference.
+        const bool first = __any_sync(0xffffffffu, m_ref == kNegInf);
+        if (first) {
+          uint32_t sr[128];
+          float mx[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
+          if (masked_tile) {
+            tmem_ld_x128(tS, sr);
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (k0 + c >= limit) sr[c] = __float_as_uint(kNegInf);
+            for (int c = 0; c < 128; ++c)
+              if (k0 + c >= limit) sr[c] = __float_as_uint(kNegInf);
 #pragma unroll
-          for (int c = 0; c < 128; c += 8) {
-            mx[0] = max3(mx[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-            mx[1] = max3(mx[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
-            mx[2] = max3(mx[2], __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
-            mx[3] = max3(mx[3], __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+            for (int c = 0; c < 128; c += 8) {
+              mx[0] = max3(mx[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+              mx[1] = max3(mx[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+              mx[2] = max3(mx[2], __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+              mx[3] = max3(mx[3], __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+            }
+          } else {
+            tmem_ld_x64(tS, *reinterpret_cast<uint32_t(*)[64]>(sr));
+            tmem_ld_x64_nowait(tS + 64, sr + 64);
+#pragma unroll
+            for (int c = 0; c < 64; c += 8) {
+              mx[0] = max3(mx[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+              mx[1] = max3(mx[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+              mx[2] = max3(mx[2], __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+              mx[3] = max3(mx[3], __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+            }
+            tmem_wait_ld_dep64(sr + 64);
+#pragma unroll
+            for (int c = 64; c < 128; c += 8) {
+              mx[0] = max3(mx[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+              mx[1] = max3(mx[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+              mx[2] = max3(mx[2], __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+              mx[3] = max3(mx[3], __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+            }
           }
-        } else {
-          tmem_ld_x64(tS, *reinterpret_cast<uint32_t(*)[64]>(sr));
-          tmem_ld_x64_nowait(tS + 64, sr + 64);
-#pragma unroll
-          for (int c = 0; c < 64; c += 8) {
-            mx[0] = max3(mx[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-            mx[1] = max3(mx[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
-            mx[2] = max3(mx[2], __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
-            mx[3] = max3(mx[3], __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+          const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+          const float m_new = fmaxf(m_ref, m_tile);
+          float alpha = 1.f;
+          bool resc = false;
+          if (m_ref == kNegInf) {
+            m_ref = m_new;
+          } else if (m_new > m_ref + kTau) {
+            alpha = ex2(m_ref - m_new);
+            l *= alpha;
+            m_ref = m_new;
+            resc = true;
           }
-          tmem_wait_ld_dep64(sr + 64);
+          if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
-          for (int c = 64; c < 128; c += 8) {
-            mx[0] = max3(mx[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-            mx[1] = max3(mx[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
-            mx[2] = max3(mx[2], __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
-            mx[3] = max3(mx[3], __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+            for (int c = 0; c < 4; ++c) {
+              uint32_t orr[32];
+              tmem_ld_x32(tO + 32 * c, orr);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+              tmem_st_x32(tO + 32 * c, orr);
+            }
           }
         }
-        const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
-        const float m_new = fmaxf(m_ref, m_tile);
-        float alpha = 1.f;
-        bool resc = false;
-        if (m_ref == kNegInf) {
-          m_ref = m_new;
-        } else if (m_new > m_ref + kTau) {
-          alpha = ex2(m_ref - m_new);
-          l *= alpha;
-          m_ref = m_new;
-          resc = true;
-        }
-        if (__any_sync(0xffffffffu, resc)) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t orr[32];
-            tmem_ld_x32(tO + 32 * c, orr);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-            tmem_st_x32(tO + 32 * c, orr);
-          }
-        }
-        const float nref = (m_ref == kNegInf) ? 0.f : -m_ref;
+        float nref = (m_ref == kNegInf) ? 0.f : -m_ref;
         // pass 2, rolled over four 32-column chunks (S reloaded from TMEM), each
         // chunk two-phase: all scale/subtracts, then 32 independent exp2, then
         // the sums and bf16 packs -- so the MUFU latency is covered
@@ -461,25 +470,78 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
           uint32_t sc[32], pk[16];
-          float pv[32];
+          float cs[4];
           tmem_ld_x32(tS + 32 * ch, sc);
           if (masked_tile) {
 #pragma unroll
             for (int e = 0; e < 32; ++e)
               if (k0 + 32 * ch + e >= limit) sc[e] = __float_as_uint(kNegInf);
           }
+          auto exp_chunk = [&]() {
+            float pv[32];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            fma2(pv[2 * i], pv[2 * i + 1], __uint_as_float(sc[2 * i]), __uint_as_float(sc[2 * i + 1]),
-                 sl2, sl2, nref, nref);
+            for (int i = 0; i < 16; ++i)
+              fma2(pv[2 * i], pv[2 * i + 1], __uint_as_float(sc[2 * i]),
+                   __uint_as_float(sc[2 * i + 1]), sl2, sl2, nref, nref);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) pv[e] = ex2(pv[e]);
+            for (int e = 0; e < 32; ++e) pv[e] = ex2(pv[e]);
+            cs[0] = cs[1] = cs[2] = cs[3] = 0.f;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            add2(la[2 * (i & 1)], la[2 * (i & 1) + 1], pv[2 * i], pv[2 * i + 1]);
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(pv[2 * i], pv[2 * i + 1]);
-            pk[i] = *reinterpret_cast<uint32_t*>(&h2);
+            for (int i = 0; i < 16; ++i) {
+              add2(cs[2 * (i & 1)], cs[2 * (i & 1) + 1], pv[2 * i], pv[2 * i + 1]);
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(pv[2 * i], pv[2 * i + 1]);
+              pk[i] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+          };
+          exp_chunk();
+          if (!first) {
+            const bool over = !((cs[0] + cs[1]) + (cs[2] + cs[3]) <= kSumLimit);
+            if (__any_sync(0xffffffffu, over)) {
+              // Raise the reference by a whole number k of binades, enough that
+              // no term of this chunk exceeds 1.  Everything already formed
+              // against the old reference (l, the stored P chunks, O~) is
+              // multiplied by 2^-k, which is exact.
+              float kr = 0.f;
+              if (over) {
+                float mc = kNegInf;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) mc = fmaxf(mc, __uint_as_float(sc[e]));
+                kr = fmaxf(ceilf(fmaf(mc, sl2, nref)), 0.f);
+              }
+              // 2^-k exactly; k >= 127 leaves nothing representable (flush to 0)
+              const float alpha = kr >= 127.f ? 0.f : __int_as_float((127 - static_cast<int>(kr)) << 23);
+              m_ref += kr;
+              nref = -m_ref;
+              l *= alpha;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) la[i] *= alpha;
+              tmem_wait_st();
+              for (int c2 = 0; c2 < ch; ++c2) {
+                uint32_t pp[16];
+                tmem_ld_x16(tS + 16 * c2, pp);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                  const float f0 = __uint_as_float(pp[e] << 16) * alpha;
+                  const float f1 = __uint_as_float(pp[e] & 0xffff0000u) * alpha;
+                  __nv_bfloat162 h2 = __floats2bfloat162_rn(f0, f1);
+                  pp[e] = *reinterpret_cast<uint32_t*>(&h2);
+                }
+                tmem_st_x16_nowait(tS + 16 * c2, pp);
+              }
+              // O~'s last update (P V of the previous tile) completed before S
+#pragma unroll 1
+              for (int c = 0; c < 4; ++c) {
+                uint32_t orr[32];
+                tmem_ld_x32(tO + 32 * c, orr);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                tmem_st_x32(tO + 32 * c, orr);
+              }
+              exp_chunk();
+            }
           }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) la[i] += cs[i];
           tmem_st_x16_nowait(tS + 16 * ch, pk);
         }
         tmem_wait_st();

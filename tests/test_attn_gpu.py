@@ -113,6 +113,23 @@ def test_masked_keys_contribute_exactly_zero(cuda_ok):
     check(*outs[0], *oracle_of(case))
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_growing_scores(cuda_ok, causal):
+    """Scores whose row maximum keeps growing from tile to tile: moderate growth
+    (the reference is raised by a few binades, already-formed terms rescaled),
+    and jumps so large that everything before them underflows to zero."""
+    B, H, N = 2, 2, 1000
+    case = W.attention(23, B, H, N, N, 128, causal, (700, N))
+    k = case.k.float()
+    grow = torch.linspace(1.0, 12.0, N).view(1, 1, N, 1)      # steady growth
+    k = k * grow
+    k[0, :, 600] *= 40.0     # one huge key in a late tile (batch 0)
+    k[1, 1, 300:310] *= 25.0  # a block of large keys mid-row
+    case.k = k.to(torch.bfloat16)
+    o, lse = run(case)
+    check(o, lse, *oracle_of(case))
+
+
 def test_deterministic(cuda_ok):
     case = W.attention(25, 2, 4, 1000, 1000, 128, True, (500, 1000))
     a, b = run(case), run(case)
