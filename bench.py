@@ -321,7 +321,8 @@ def reduce_max(times: dict, world: int, device) -> dict:
 def profile_case(spec: str, iters: int):
     """Run one operation `iters` times on a given shape (for ncu captures).
 
-    spec: "attn:B,H,N[,causal]" | "softmax:rows,cols" | "decode:B,H,Nk[,splits]"
+    spec: "attn:B,H,N[,causal]" | "attnqk:B,H,N[,causal]" (QK-norm inputs with
+          their score bound) | "softmax:rows,cols" | "decode:B,H,Nk[,splits]"
           | "append:B,H,Nk,n_new[,splits]".
     Inputs come from the same generators as the full workloads.
     """
@@ -337,6 +338,20 @@ def profile_case(spec: str, iters: int):
         q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
         kl = c.key_len.to(dev) if c.key_len is not None else None
         run = lambda: osm.attn_fwd(q, k, v, c.scale, causal, kl)
+        work = attn_flops(B, H, N, N, 128, causal, None if kl is None else c.key_len.numpy())
+        unit = "TFLOP/s"
+    elif op == "attnqk":
+        # QK-norm inputs (q, k rows scaled to norm sqrt(d)) with their known
+        # score bound scale * max|q| * max|k|, through osm_attn_fwd_bounded
+        B, H, N = (int(x) for x in parts[:3])
+        causal = len(parts) > 3 and parts[3] == "causal"
+        c = W.attention(4, B, H, N, N, 128, causal, (N // 2, N) if causal else None)
+        q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
+        q = (q.float() / q.float().norm(dim=-1, keepdim=True) * 128 ** 0.5).to(torch.bfloat16)
+        k = (k.float() / k.float().norm(dim=-1, keepdim=True) * 128 ** 0.5).to(torch.bfloat16)
+        bound = c.scale * float(q.float().norm(dim=-1).max()) * float(k.float().norm(dim=-1).max())
+        kl = c.key_len.to(dev) if c.key_len is not None else None
+        run = lambda: osm.attn_fwd(q, k, v, c.scale, causal, kl, score_bound=bound)
         work = attn_flops(B, H, N, N, 128, causal, None if kl is None else c.key_len.numpy())
         unit = "TFLOP/s"
     elif op == "softmax":

@@ -35,6 +35,7 @@ _P, _I, _I64, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_
 SIGNATURES = {
     "osm_softmax_rows": (_I, [_P, _P, _I64, _I64, _P]),
     "osm_attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P]),
+    "osm_attn_fwd_bounded": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _F, _P]),
     "osm_attn_decode_splitkv_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "osm_attn_decode_splitkv": (_I, [_I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _I, _P, _SZ, _P]),
     "osm_attn_decode_splitkv_noalloc": (_I, [_I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _I, _P]),
@@ -115,10 +116,12 @@ def softmax_rows(x: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.T
     return y
 
 
-def attn_fwd(q, k, v, scale=None, causal=False, key_len=None, out=None, lse=None):
+def attn_fwd(q, k, v, scale=None, causal=False, key_len=None, out=None, lse=None,
+             score_bound=None):
     """Attention forward.  q [B,H,Nq,d], k, v [B,H,Nk,d] bf16 CUDA; key_len int32 [B] or None.
 
-    Returns (o [B,H,Nq,d] bf16, lse [B,H,Nq] fp32).
+    Returns (o [B,H,Nq,d] bf16, lse [B,H,Nq] fp32).  `score_bound`: a known
+    upper bound on the scaled scores (osm_attn_fwd_bounded); None = unknown.
     """
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, torch.bfloat16, q.device)
@@ -142,9 +145,16 @@ def attn_fwd(q, k, v, scale=None, causal=False, key_len=None, out=None, lse=None
         kl = key_len.data_ptr()
     lib = load_library()
     with torch.cuda.device(q.device):
-        _check(lib.osm_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                lse_t.data_ptr(), B, H, Nq, Nk, d, float(scale), int(bool(causal)),
-                                kl, _stream(q)), "osm_attn_fwd")
+        if score_bound is None:
+            _check(lib.osm_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                    lse_t.data_ptr(), B, H, Nq, Nk, d, float(scale),
+                                    int(bool(causal)), kl, _stream(q)), "osm_attn_fwd")
+        else:
+            _check(lib.osm_attn_fwd_bounded(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                            o.data_ptr(), lse_t.data_ptr(), B, H, Nq, Nk, d,
+                                            float(scale), int(bool(causal)), kl,
+                                            float(score_bound), _stream(q)),
+                   "osm_attn_fwd_bounded")
     return o, lse_t
 
 

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <limits>
 #include <cstdint>
 
 #include "internal.h"
@@ -45,9 +46,10 @@ osm_status osm_softmax_rows(const float* x, float* y, int64_t rows, int64_t cols
   return from_cuda(osm::launch_softmax_rows(x, y, rows, cols, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-osm_status osm_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                        int H, int Nq, int Nk, int d, float scale, int causal,
-                        const int32_t* key_len, osm_stream_t stream) {
+namespace {
+osm_status attn_fwd_checked(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                            const int32_t* key_len, float score_bound, osm_stream_t stream) {
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return OSM_ERR_INVALID_VALUE;
   if (causal != 0 && causal != 1) return OSM_ERR_INVALID_VALUE;
   if (!(scale > 0.f) || !std::isfinite(scale)) return OSM_ERR_INVALID_VALUE;
@@ -60,9 +62,26 @@ osm_status osm_attn_fwd(const void* q, const void* k, const void* v, void* o, fl
   if (static_cast<int64_t>(B) * H > 0x7fffffffLL) return OSM_ERR_UNSUPPORTED;
   bool tmap_ok = true;
   cudaError_t e = osm::launch_attn_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, key_len,
-                                       reinterpret_cast<cudaStream_t>(stream), &tmap_ok);
+                                       score_bound, reinterpret_cast<cudaStream_t>(stream),
+                                       &tmap_ok);
   if (!tmap_ok) return OSM_ERR_UNSUPPORTED;  // shape the TMA descriptor cannot express
   return from_cuda(e);
+}
+}  // namespace
+
+osm_status osm_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int H, int Nq, int Nk, int d, float scale, int causal,
+                        const int32_t* key_len, osm_stream_t stream) {
+  return attn_fwd_checked(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, key_len,
+                          std::numeric_limits<float>::quiet_NaN(), stream);
+}
+
+osm_status osm_attn_fwd_bounded(const void* q, const void* k, const void* v, void* o, float* lse,
+                                int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                                const int32_t* key_len, float score_bound, osm_stream_t stream) {
+  if (!std::isfinite(score_bound) || std::fabs(score_bound) > 1e30f) return OSM_ERR_INVALID_VALUE;
+  return attn_fwd_checked(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, key_len, score_bound,
+                          stream);
 }
 
 size_t osm_attn_decode_splitkv_workspace_bytes(int B, int H, int d, int num_splits) {

@@ -21,22 +21,26 @@
 //   warp 1     MMA issuer (one thread): S_t = Q_t K_j^T into TMEM, then
 //              O~_t += P_t V_j with P_t read straight from TMEM.
 //   warps 4-7  softmax for query tile 0; warps 8-11 for tile 1.  One thread
-//              per query row.  Pass 1: the row's 128 scores TMEM -> registers,
-//              mask, row max.  Pass 2, a rolled loop over four 32-column
-//              chunks (small code, no register spills): reload the chunk from
-//              TMEM, scale and subtract in packed f32x2, 32 independent exp2
-//              (so the MUFU latency is covered), row sum, bf16 pack, store P
-//              over the S columns already consumed.  Rescale O~ in TMEM when
-//              the max has grown; epilogue O = O~ / l, lse.
+//              per query row, a rolled loop over four 32-column chunks (small
+//              code, no register spills): the chunk TMEM -> registers, mask,
+//              scale and subtract the reference in packed f32x2, 32
+//              independent exp2 (so the MUFU latency is covered), row sum,
+//              bf16 pack, store P over the S columns already consumed;
+//              epilogue O = O~ / l, lse.
 //   TMEM       512 columns: S_0 | S_1 | O~_0 | O~_1 (128 fp32 columns each).
-// The rescale is taken only when the new max exceeds the reference by more
-// than kTau (base-2 units); every identity of the recurrence holds for any
-// common reference ("Precision, and what can still go wrong", second point),
-// so skipping a small rescale changes no result, it only lets P reach 2^kTau.
+// The reference subtracted before exp2 need not be the running maximum: every
+// identity of the recurrence holds for any common reference ("Precision, and
+// what can still go wrong", second point: any bound on the scores will do).
+// So only a row's first tile looks for the maximum (or none, when the caller
+// knows a bound and the row starts there).  After that the reference moves by
+// whole binades only when a chunk would otherwise hold a term above 2^16
+// (raise: everything formed so far is scaled by an exact power of two) or
+// when all of a row's terms so far underflow (lower).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstdint>
 
 #include "internal.h"
@@ -56,10 +60,11 @@ constexpr int kItemSlots = 4;  // depth of the CTA's queue of work-item numbers
 constexpr uint32_t kTileBytes = kRows * kHeadDim * 2;  // 32768
 constexpr uint32_t kBoxBytes = 128 * 64 * 2;           // one TMA box: 64 columns x 128 rows
 constexpr int kThreads = 384;
-constexpr float kTau = 8.0f;
-// Tiles after a row's first skip the max: a 32-term chunk whose sum stays at
-// or below kSumLimit has no term above it (all terms are >= 0), so P <= 2^16.
+// A 32-term chunk whose sum stays at or below kSumLimit has no term above it
+// (all terms are >= 0), so every P is at most 2^16 times the reference's term.
 constexpr float kSumLimit = 65536.0f;
+// A row's first tile may leave the reference up to kTau below the maximum.
+constexpr float kTau = 8.0f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNegInf = -__builtin_huge_valf();
 
@@ -104,6 +109,7 @@ struct Params {
   int npairs;
   int num_items;
   float scale_log2;
+  float m_init;  // starting reference of every row, base-2 units of the scaled scores
   const int32_t* key_len;
   __nv_bfloat16* o;
   float* lse;
@@ -141,6 +147,9 @@ __device__ unsigned int g_err_word;
 constexpr int kCounters = 1024;
 __device__ unsigned int g_item_counter[kCounters];
 
+// kBounded: every row starts from the caller's bound (p.m_init finite), so no
+// tile looks for the maximum and an all-underflow start can lower the reference.
+template <bool kBounded>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -393,7 +402,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int limit = it.kv_len;
       if (p.causal) limit = min(limit, row + 1 + (p.Nk - p.Nq));
-      float m_ref = kNegInf, l = 0.f;
+      // Every row starts from the reference p.m_init (base-2 units): -inf, so
+      // that a row's first tile takes its maximum, or a bound the caller
+      // knows.  Later tiles form their terms against the current reference
+      // without looking for the maximum: a chunk with a term that may exceed
+      // kSumLimit raises the reference, a chunk whose terms all underflow
+      // while nothing has accumulated yet lowers it.
+      float m_ref = kBounded ? p.m_init : kNegInf, l = 0.f;
       for (int j = 0; j < it.n_kv; ++j) {
         ok = wait_all(bar(S_FULL + t), sf_ph, kSite | 7);
         if (!ok) break;
@@ -401,10 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const int k0 = j * kKeys;
         const bool masked_tile = __any_sync(0xffffffffu, k0 + kKeys > limit);
-        // A row's first tile (no reference yet) takes the tile max first.  Later
-        // tiles go straight to the exponentials against the current reference;
-        // a chunk whose sum shows a term above kSumLimit raises the reference.
-        const bool first = __any_sync(0xffffffffu, m_ref == kNegInf);
+        const bool first = !kBounded && __any_sync(0xffffffffu, m_ref == kNegInf);
         if (first) {
           uint32_t sr[128];
           float mx[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
@@ -463,9 +475,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         float nref = (m_ref == kNegInf) ? 0.f : -m_ref;
-        // pass 2, rolled over four 32-column chunks (S reloaded from TMEM), each
-        // chunk two-phase: all scale/subtracts, then 32 independent exp2, then
-        // the sums and bf16 packs -- so the MUFU latency is covered
+        // pass over four 32-column chunks (S read from TMEM), each chunk
+        // two-phase: all scale/subtracts, then 32 independent exp2, then the
+        // sums and bf16 packs -- so the MUFU latency is covered
         float la[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
@@ -495,21 +507,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           };
           exp_chunk();
           if (!first) {
-            const bool over = !((cs[0] + cs[1]) + (cs[2] + cs[3]) <= kSumLimit);
+            bool over = !((cs[0] + cs[1]) + (cs[2] + cs[3]) <= kSumLimit);
+            if constexpr (kBounded)  // every term underflowed and nothing has accumulated
+              over = over || ((cs[0] + cs[1]) + (cs[2] + cs[3]) == 0.f && l == 0.f &&
+                              (la[0] + la[1]) + (la[2] + la[3]) == 0.f);
             if (__any_sync(0xffffffffu, over)) {
-              // Raise the reference by a whole number k of binades, enough that
-              // no term of this chunk exceeds 1.  Everything already formed
-              // against the old reference (l, the stored P chunks, O~) is
-              // multiplied by 2^-k, which is exact.
+              // Move the reference by a whole number k of binades so that this
+              // chunk's largest term is 1.  Raising (k > 0) multiplies
+              // everything already formed against the old reference (l, the
+              // stored P chunks, O~) by 2^-k, which is exact.  Lowering (only
+              // with a caller's bound) happens while nothing has accumulated.
               float kr = 0.f;
               if (over) {
                 float mc = kNegInf;
 #pragma unroll
                 for (int e = 0; e < 32; ++e) mc = fmaxf(mc, __uint_as_float(sc[e]));
-                kr = fmaxf(ceilf(fmaf(mc, sl2, nref)), 0.f);
+                if constexpr (kBounded) {
+                  if (mc != kNegInf) kr = ceilf(fmaf(mc, sl2, nref));
+                } else {
+                  kr = fmaxf(ceilf(fmaf(mc, sl2, nref)), 0.f);
+                }
               }
               // 2^-k exactly; k >= 127 leaves nothing representable (flush to 0)
-              const float alpha = kr >= 127.f ? 0.f : __int_as_float((127 - static_cast<int>(kr)) << 23);
+              const float alpha = (kBounded && kr <= 0.f) ? 1.f
+                                  : (kr >= 127.f ? 0.f : __int_as_float((127 - static_cast<int>(kr)) << 23));
               m_ref += kr;
               nref = -m_ref;
               l *= alpha;
@@ -529,6 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st_x16_nowait(tS + 16 * c2, pp);
               }
               // O~'s last update (P V of the previous tile) completed before S
+              // (before a row's first P V it holds no value: scaling it is harmless)
 #pragma unroll 1
               for (int c = 0; c < 4; ++c) {
                 uint32_t orr[32];
@@ -607,7 +629,8 @@ int sm_count_current_device() {
 
 cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                             int B, int H, int Nq, int Nk, int d, float scale, int causal,
-                            const int32_t* key_len, cudaStream_t s, bool* tmap_ok) {
+                            const int32_t* key_len, float score_bound, cudaStream_t s,
+                            bool* tmap_ok) {
   using namespace attn;
   *tmap_ok = true;
   (void)d;
@@ -636,6 +659,11 @@ cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o
   const int64_t items = static_cast<int64_t>(BH) * p.npairs;
   p.num_items = static_cast<int>(items);
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  // a known bound on the scaled scores starts every row there; without one a
+  // row's first tile takes its maximum
+  p.m_init = std::isfinite(score_bound)
+                 ? static_cast<float>(static_cast<double>(score_bound) * 1.4426950408889634)
+                 : kNegInf;
   p.key_len = key_len;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
@@ -657,14 +685,20 @@ cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(attr_done & bit)) {
-    e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(attn_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(attn_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
     attr_done |= bit;
   }
   const int grid = static_cast<int>(items < sm_count_current_device() ? items
                                                                       : sm_count_current_device());
-  attn_fwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+  if (std::isfinite(score_bound))
+    attn_fwd_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+  else
+    attn_fwd_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 

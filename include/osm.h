@@ -79,10 +79,13 @@ osm_status osm_softmax_rows(const float *x, float *y, int64_t rows, int64_t cols
  *          (causal and j > i + (Nk - Nq))   (causal is bottom-right aligned),
  *   o_i = softmax(s_i) V,   lse_i = log sum_j exp(s_ij).
  * Computed tile by tile ([P3] "Blocks, the bridge to FlashAttention"): 128
- * query rows against streamed 128-key tiles, running max m, running sum l and
- * unnormalised output O~ in FP32, rescaled by 2^(m_old - m_new) when the max
- * grows, masks applied inside the tile loop ([P2] "Walking through it"), one
- * division at the end, lse = m + log l ([P3] "From weights to outputs").
+ * query rows against streamed 128-key tiles, a running reference m, running
+ * sum l and unnormalised output O~ in FP32, rescaled by 2^(m_old - m_new)
+ * when the reference moves, masks applied inside the tile loop ([P2] "Walking
+ * through it"), one division at the end, lse = m + log l ([P3] "From weights
+ * to outputs").  The reference need not be the running maximum ([P3]
+ * "Precision, and what can still go wrong": any bound will do); the kernel
+ * moves it only when a term would exceed 2^16 or all terms so far underflow.
  * No score matrix is written to memory.
  *
  *   q     [B, H, Nq, d] bf16;  k, v [B, H, Nk, d] bf16 (read only).
@@ -101,6 +104,29 @@ osm_status osm_softmax_rows(const float *x, float *y, int64_t rows, int64_t cols
 osm_status osm_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
                         int B, int H, int Nq, int Nk, int d, float scale, int causal,
                         const int32_t *key_len, osm_stream_t stream);
+
+/*
+ * osm_attn_fwd_bounded — osm_attn_fwd for scores with a known upper bound.
+ *
+ * [P3] "Precision, and what can still go wrong": any number at least as large
+ * as every score prevents overflow, so with a bound known in advance (for
+ * example queries and keys normalised by QK-norm, so |s| <= scale |q| |k|) it
+ * can be subtracted once and the running maximum is never needed.  Every row
+ * starts from `score_bound` (scaled-score units, natural log) instead of 0.
+ * With a valid bound no rescale happens unless the bound lies more than
+ * about 87 (2^126 in weight) above a row's maximum, where all terms would
+ * underflow; the kernel then lowers the reference (the pages' warning that a
+ * loose bound risks underflowing every term).  A score above the bound by
+ * more than 16 binades' worth raises it.  Either way the result is exact;
+ * the bound only decides how often a chunk is redone.
+ *
+ * Arguments as osm_attn_fwd, plus:
+ *   score_bound  finite, |score_bound| <= 1e30 (else OSM_ERR_INVALID_VALUE).
+ */
+osm_status osm_attn_fwd_bounded(const void *q, const void *k, const void *v, void *o,
+                                float *lse, int B, int H, int Nq, int Nk, int d, float scale,
+                                int causal, const int32_t *key_len, float score_bound,
+                                osm_stream_t stream);
 
 /*
  * osm_attn_decode_splitkv_workspace_bytes — bytes of device workspace that

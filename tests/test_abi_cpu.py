@@ -107,6 +107,23 @@ def test_attn_validation(lib):
     assert call(Nq=0) == osm.OSM_OK
 
 
+def test_bounded_attn_validation(lib):
+    f = lib.osm_attn_fwd_bounded
+    base = [FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 128, 128, 0.088, 0, None, 3.0, None]
+
+    def call(i, val):
+        a = list(base)
+        a[i] = val
+        return f(*a)
+
+    assert call(13, float("nan")) == osm.OSM_ERR_INVALID_VALUE     # the bound must be finite
+    assert call(13, float("inf")) == osm.OSM_ERR_INVALID_VALUE
+    assert call(13, 1e31) == osm.OSM_ERR_INVALID_VALUE
+    assert call(0, None) == osm.OSM_ERR_INVALID_VALUE              # then the usual checks
+    assert call(9, 64) == osm.OSM_ERR_UNSUPPORTED
+    assert call(5, 0) == osm.OSM_OK                                 # empty: no-op
+
+
 def test_decode_and_merge_validation(lib):
     f = lib.osm_attn_decode_splitkv
     need = osm.decode_workspace_bytes(2, 2, 128, 4)

@@ -130,6 +130,49 @@ def test_growing_scores(cuda_ok, causal):
     check(o, lse, *oracle_of(case))
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_scores_far_below_zero(cuda_ok, causal):
+    """Every score near -200: against the starting reference 0 all terms would
+    underflow, so the first chunk of each row lowers the reference."""
+    B, H, N = 1, 2, 700
+    case = W.attention(24, B, H, N, N, 128, causal, (400, N))
+    q = 4.0 + 0.05 * case.q.float()
+    k = -4.5 + 0.05 * case.k.float()
+    case.q, case.k = q.to(torch.bfloat16), k.to(torch.bfloat16)
+    o, lse = run(case)
+    ro, rl = oracle_of(case)
+    assert float(np.max(rl[np.isfinite(rl)])) < -150
+    check(o, lse, ro, rl)
+
+
+def qk_normed(seed, causal):
+    """QK-norm inputs: q and k rows scaled to norm sqrt(d), so |s| <= scale * d."""
+    B, H, N = 2, 2, 1000
+    case = W.attention(seed, B, H, N, N, 128, causal, (500, N))
+    for name in ("q", "k"):
+        t = getattr(case, name).float()
+        t = t / t.norm(dim=-1, keepdim=True) * 128 ** 0.5
+        setattr(case, name, t.to(torch.bfloat16))
+    nq = float(case.q.float().norm(dim=-1).max())
+    nk = float(case.k.float().norm(dim=-1).max())
+    return case, case.scale * nq * nk   # an upper bound of every score
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("which", ["valid", "too_low", "far_too_high"])
+def test_known_bound(cuda_ok, causal, which):
+    """Scores with a known bound (QK-norm): exact whatever the bound -- a valid
+    one, one far below the scores (the reference is raised) and one so far
+    above them that every term would underflow (the reference is lowered)."""
+    case, bound = qk_normed(25 + causal, causal)
+    bound = {"valid": bound, "too_low": -60.0, "far_too_high": bound + 400.0}[which]
+    kl = case.key_len.cuda()
+    o, lse = osm.attn_fwd(case.q.cuda(), case.k.cuda(), case.v.cuda(), case.scale, causal, kl,
+                          score_bound=bound)
+    assert osm.device_status() == 0
+    check(o, lse, *oracle_of(case))
+
+
 def test_deterministic(cuda_ok):
     case = W.attention(25, 2, 4, 1000, 1000, 128, True, (500, 1000))
     a, b = run(case), run(case)
