@@ -17,6 +17,7 @@ from .ref import (  # noqa: F401
     set_partitions,
     softmax_row_fsum,
     softmax_rows_ref,
+    softmax_topk_ref,
     summary_of,
     tiled_softmax_online,
     visible_keys,

@@ -69,6 +69,34 @@ def softmax_rows_ref(x: np.ndarray) -> np.ndarray:
     return y[0] if squeeze else y
 
 
+def softmax_topk_ref(x: np.ndarray, k: int) -> Tuple[np.ndarray, np.ndarray]:
+    """The k largest entries of every row and their softmax probabilities.
+
+    [P3] "Precision, and what can still go wrong", the `softmax_topk` exercise
+    after it (Milakov & Gimelshein's fused softmax plus top-k): the indices of
+    the k largest scores, and exp(x_i) / sum_j exp(x_j) at those indices.  The
+    page's own version is unstable; here the probabilities are the safe
+    softmax of the whole row (``softmax_rows_ref``) read at the chosen indices.
+    Order: value descending, equal values by index ascending (one total order,
+    so the result is unique).  Returns (idx int64 [R, k], prob float64 [R, k]).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    if x.ndim == 1:
+        x = x[None, :]
+    R, n = x.shape
+    if not 1 <= k <= n:
+        raise ValueError("need 1 <= k <= number of columns")
+    y = softmax_rows_ref(x)
+    idx = np.empty((R, k), dtype=np.int64)
+    prob = np.empty((R, k), dtype=np.float64)
+    cols = np.arange(n)
+    for r in range(R):
+        order = np.lexsort((cols, -x[r]))[:k]   # primary key -x, then the index
+        idx[r] = order
+        prob[r] = y[r, order]
+    return idx, prob
+
+
 def softmax_row_fsum(xs: Sequence[float]) -> List[float]:
     """Safe softmax of one short row with exactly rounded sums (math.fsum).
 

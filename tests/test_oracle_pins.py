@@ -326,3 +326,79 @@ def test_online_single_query_block_sizes():
         o, lse = O.online_attention_single(q, k, v, 0.25, block)
         assert np.allclose(o, o_def[0, 0, 0], rtol=1e-13, atol=1e-14)
         assert lse == pytest.approx(lse_def[0, 0, 0], rel=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# Fused softmax + top-k ([P3] the `softmax_topk` exercise after "Precision,
+# and what can still go wrong"; Milakov & Gimelshein's fused form).
+
+
+def _topk_bruteforce(row, k):
+    """Sort (-x_i, i) with Python's sort; probabilities with math.exp / fsum."""
+    n = len(row)
+    order = sorted(range(n), key=lambda i: (-row[i], i))[:k]
+    finite = [v for v in row if v != -math.inf]
+    if not finite:
+        return order, [0.0] * k
+    mx = max(finite)
+    total = math.fsum(math.exp(v - mx) for v in finite)
+    return order, [(math.exp(row[i] - mx) / total if row[i] != -math.inf else 0.0)
+                   for i in order]
+
+
+def test_topk_matches_the_pages_naive_formula():
+    """On moderate values with no ties, the page's own (unstable) formula
+    idx = argsort(-x)[:k], exp(x[idx]) / sum exp(x) is exact enough to pin."""
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal((5, 300)) * 3
+    for k in (1, 4, 17, 300):
+        idx, prob = O.softmax_topk_ref(x, k)
+        for r in range(5):
+            naive_idx = np.argsort(-x[r])[:k]
+            naive_p = np.exp(x[r][naive_idx]) / np.exp(x[r]).sum()
+            assert np.array_equal(idx[r], naive_idx)
+            assert np.allclose(prob[r], naive_p, rtol=1e-13, atol=0)
+
+
+def test_topk_bruteforce_ties_and_masked_entries():
+    rng = np.random.default_rng(32)
+    x = rng.integers(-3, 4, size=(6, 40)).astype(np.float64)   # many ties
+    x[1, ::3] = -np.inf
+    x[2, :] = -np.inf                                           # an all -inf row
+    x[3, :] = 2.0                                               # all equal
+    for k in (1, 3, 8, 40):
+        idx, prob = O.softmax_topk_ref(x, k)
+        for r in range(6):
+            bi, bp = _topk_bruteforce(list(x[r]), k)
+            assert list(idx[r]) == bi
+            assert np.allclose(prob[r], bp, rtol=1e-14, atol=0)
+    idx, prob = O.softmax_topk_ref(x, 40)
+    assert list(idx[3]) == list(range(40))                      # ties: lowest index first
+    assert np.all(prob[2] == 0)
+    assert math.fsum(prob[0]) == pytest.approx(1.0, abs=1e-14)  # k = n: all the mass
+    assert np.all(np.diff(prob[0]) <= 0)                        # probabilities non-increasing
+
+
+def test_topk_is_stable_where_the_naive_formula_overflows():
+    x = np.array([[1000.0, 999.0, 998.0, 0.0]])
+    with np.errstate(over="ignore", invalid="ignore"):
+        naive = np.exp(x[0][:2]) / np.exp(x[0]).sum()
+    assert np.all(np.isnan(naive))                              # inf / inf
+    idx, prob = O.softmax_topk_ref(x, 2)
+    assert list(idx[0]) == [0, 1]
+    e = np.exp([0.0, -1.0, -2.0, -1000.0])
+    assert np.allclose(prob[0], e[:2] / e.sum(), rtol=1e-15)
+
+
+def test_planted_topk_bugs_are_caught():
+    """Plausible slips (ties broken by the higher index, probabilities
+    normalised over the k chosen entries only) fail the brute-force pin."""
+    x = np.array([[1.0, 3.0, 3.0, 0.5, 2.0]])
+    bi, bp = _topk_bruteforce(list(x[0]), 3)
+    idx, prob = O.softmax_topk_ref(x, 3)
+    assert list(idx[0]) == bi == [1, 2, 4]
+    wrong_ties = list(np.lexsort((-np.arange(5), -x[0]))[:3])
+    assert wrong_ties != bi
+    wrong_norm = np.exp(x[0][bi]) / np.exp(x[0][bi]).sum()
+    assert not np.allclose(wrong_norm, bp, rtol=1e-3)
+    assert np.allclose(prob[0], bp, rtol=1e-14)
