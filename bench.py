@@ -322,7 +322,8 @@ def profile_case(spec: str, iters: int):
     """Run one operation `iters` times on a given shape (for ncu captures).
 
     spec: "attn:B,H,N[,causal]" | "attnqk:B,H,N[,causal]" (QK-norm inputs with
-          their score bound) | "softmax:rows,cols" | "decode:B,H,Nk[,splits]"
+          their score bound) | "softmax:rows,cols" | "topk:rows,cols,k"
+          | "decode:B,H,Nk[,splits]"
           | "append:B,H,Nk,n_new[,splits]".
     Inputs come from the same generators as the full workloads.
     """
@@ -360,6 +361,13 @@ def profile_case(spec: str, iters: int):
         y = torch.empty_like(x)
         run = lambda: osm.softmax_rows(x, out=y)
         work, unit = 8 * R * C, "GB/s"
+    elif op == "topk":
+        R, C, kk = (int(x) for x in parts[:3])
+        x = W.softmax_logits(2, rows=R, cols=C).to(dev)
+        ii = torch.empty((R, kk), dtype=torch.int32, device=dev)
+        pp = torch.empty((R, kk), dtype=torch.float32, device=dev)
+        run = lambda: osm.softmax_topk(x, kk, idx=ii, prob=pp)
+        work, unit = 4 * R * C + 8 * R * kk, "GB/s"
     elif op == "decode":
         B, H, Nk = (int(x) for x in parts[:3])
         S = int(parts[3]) if len(parts) > 3 else 16

@@ -34,6 +34,7 @@ OSM_F32, OSM_BF16 = 0, 1
 _P, _I, _I64, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
 SIGNATURES = {
     "osm_softmax_rows": (_I, [_P, _P, _I64, _I64, _P]),
+    "osm_softmax_topk": (_I, [_P, _I64, _I64, _I, _P, _P, _P]),
     "osm_attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P]),
     "osm_attn_fwd_bounded": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _F, _P]),
     "osm_attn_decode_splitkv_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
@@ -114,6 +115,27 @@ def softmax_rows(x: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.T
         _check(lib.osm_softmax_rows(x.data_ptr(), y.data_ptr(), x.shape[0], x.shape[1],
                                     _stream(x)), "osm_softmax_rows")
     return y
+
+
+def softmax_topk(x, k, idx=None, prob=None):
+    """Top-k of every row of x ([rows, cols] fp32 CUDA) with softmax probabilities.
+
+    Returns (idx [rows, k] int32, prob [rows, k] fp32): larger value first,
+    ties by smaller column.
+    """
+    _need(x, "x", torch.float32)
+    if x.dim() != 2:
+        raise ValueError("x must be [rows, cols]")
+    rows, cols = x.shape
+    idx_t = torch.empty((rows, k), dtype=torch.int32, device=x.device) if idx is None else idx
+    prob_t = torch.empty((rows, k), dtype=torch.float32, device=x.device) if prob is None else prob
+    _need(idx_t, "idx", torch.int32, x.device)
+    _need(prob_t, "prob", torch.float32, x.device)
+    lib = load_library()
+    with torch.cuda.device(x.device):
+        _check(lib.osm_softmax_topk(x.data_ptr(), rows, cols, int(k), idx_t.data_ptr(),
+                                    prob_t.data_ptr(), _stream(x)), "osm_softmax_topk")
+    return idx_t, prob_t
 
 
 def attn_fwd(q, k, v, scale=None, causal=False, key_len=None, out=None, lse=None,

@@ -46,6 +46,19 @@ osm_status osm_softmax_rows(const float* x, float* y, int64_t rows, int64_t cols
   return from_cuda(osm::launch_softmax_rows(x, y, rows, cols, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+osm_status osm_softmax_topk(const float* x, int64_t rows, int64_t cols, int k, int32_t* idx,
+                            float* prob, osm_stream_t stream) {
+  if (rows < 0 || cols < 0) return OSM_ERR_INVALID_VALUE;
+  if (rows == 0) return OSM_OK;
+  if (k < 1 || k > cols) return OSM_ERR_INVALID_VALUE;
+  if (k > 32) return OSM_ERR_UNSUPPORTED;
+  if (cols > 0x7fffffffLL || rows > (int64_t{1} << 28)) return OSM_ERR_UNSUPPORTED;
+  if (!x || !idx || !prob || !aligned4(x) || !aligned4(idx) || !aligned4(prob))
+    return OSM_ERR_INVALID_VALUE;
+  return from_cuda(osm::launch_softmax_topk(x, rows, cols, k, idx, prob,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
 namespace {
 osm_status attn_fwd_checked(const void* q, const void* k, const void* v, void* o, float* lse,
                             int B, int H, int Nq, int Nk, int d, float scale, int causal,

@@ -14,6 +14,10 @@ int sm_count_current_device();
 cudaError_t launch_softmax_rows(const float* x, float* y, int64_t rows, int64_t cols,
                                 cudaStream_t s);
 
+// softmax_topk.cu
+cudaError_t launch_softmax_topk(const float* x, int64_t rows, int64_t cols, int k, int32_t* idx,
+                                float* prob, cudaStream_t s);
+
 // attn_fwd.cu
 cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                             int B, int H, int Nq, int Nk, int d, float scale, int causal,

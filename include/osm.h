@@ -72,6 +72,31 @@ osm_status osm_softmax_rows(const float *x, float *y, int64_t rows, int64_t cols
                             osm_stream_t stream);
 
 /*
+ * osm_softmax_topk — the k largest entries of every row of an fp32 matrix and
+ * their softmax probabilities, from one read of the row.
+ *
+ * Defines ([P3] the `softmax_topk` exercise after "Precision, and what can
+ * still go wrong", Milakov & Gimelshein's fused softmax + top-k): for row r,
+ * idx[r, 0..k-1] are the columns of the k largest x[r, :], in the order
+ * larger value first, equal values by smaller column (a total order, so the
+ * result is unique), and prob[r, t] = exp(x[r, idx[r, t]] - m_r) / l_r with
+ * the row's (m_r, l_r) as in osm_softmax_rows.  Computed in one pass: every
+ * thread keeps the online normaliser (m, l) and a sorted list of its k best
+ * (value, column) pairs; both merge exactly in any grouping ([P3] "Merging
+ * partial results"), warp by warp, then across a thread-block cluster.
+ *
+ *   x     [rows, cols] fp32, device, read only; entries finite or -inf.
+ *   idx   [rows, k] int32 (written);  prob [rows, k] fp32 (written).
+ *   rows >= 0 (0 is a no-op), 1 <= k <= cols; k <= 32 (larger k returns
+ *   OSM_ERR_UNSUPPORTED: each thread's list lives in registers); cols <= 2^31 - 1;
+ *   rows <= 2^28.
+ * An all -inf row gives idx = 0..k-1 and prob = 0.  x, idx, prob 4-byte
+ * aligned; 16-byte aligned x with cols % 4 == 0 takes the vector-load path.
+ */
+osm_status osm_softmax_topk(const float *x, int64_t rows, int64_t cols, int k, int32_t *idx,
+                            float *prob, osm_stream_t stream);
+
+/*
  * osm_attn_fwd — exact softmax attention forward, BF16 in, FP32 state.
  *
  * Defines: for every (b, h) and query row i,

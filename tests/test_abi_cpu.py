@@ -78,6 +78,18 @@ def test_softmax_validation(lib):
     assert f(None, None, 4, 0, None) == osm.OSM_OK
 
 
+def test_softmax_topk_validation(lib):
+    f = lib.osm_softmax_topk
+    assert f(None, 4, 100, 8, FAKE, FAKE, None) == osm.OSM_ERR_INVALID_VALUE
+    assert f(FAKE, 4, 100, 8, None, FAKE, None) == osm.OSM_ERR_INVALID_VALUE
+    assert f(FAKE, 4, 100, 0, FAKE, FAKE, None) == osm.OSM_ERR_INVALID_VALUE    # k < 1
+    assert f(FAKE, 4, 5, 6, FAKE, FAKE, None) == osm.OSM_ERR_INVALID_VALUE      # k > cols
+    assert f(FAKE, 4, 100, 33, FAKE, FAKE, None) == osm.OSM_ERR_UNSUPPORTED     # k > 32
+    assert f(FAKE + 2, 4, 100, 8, FAKE, FAKE, None) == osm.OSM_ERR_INVALID_VALUE
+    assert f(FAKE, -1, 100, 8, FAKE, FAKE, None) == osm.OSM_ERR_INVALID_VALUE
+    assert f(None, 0, 100, 8, None, None, None) == osm.OSM_OK                   # empty: no-op
+
+
 def test_attn_validation(lib):
     f = lib.osm_attn_fwd
     ok_args = [FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 128, 128, 0.088, 0, None, None]
