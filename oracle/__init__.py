@@ -7,6 +7,7 @@ from .ref import (  # noqa: F401
     NEG_INF,
     all_orders_and_groupings,
     attention_bruteforce,
+    attention_bwd_ref,
     attention_ref,
     finalize,
     lse_merge_ref,

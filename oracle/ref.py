@@ -315,6 +315,57 @@ def attention_ref(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
     return o, lse
 
 
+def attention_bwd_ref(q, k, v, o, lse, do, scale: float, causal: bool = False,
+                      key_len=None, parts: bool = False):
+    """Gradients of softmax attention in float64, from the forward's o and lse.
+
+    [P3] "From weights to outputs": the log-sum-exp is all the backward pass
+    needs to rebuild the weights, p_ij = exp(s_ij - lse_i).  With the masks of
+    ``attention_ref`` (p = 0 where masked, and for a row with lse = -inf):
+        dV = P^T dO,  dP = dO V^T,  D_i = sum_c dO_ic O_ic,
+        dS = P * (dP - D_i),  dQ = scale dS K,  dK = scale dS^T Q.
+    These are the derivatives of sum(dO * O) for O = softmax(s) V; the pins
+    check them against finite differences of ``attention_ref``.
+    Returns (dq, dk, dv) float64; with ``parts`` also, per (b, h), the
+    arrays (|P|^T |dO|, scale |dS| |K|, scale |dS|^T |Q|) that bound the
+    rounding of the terms (used for the GPU tolerance).
+    """
+    q, k, v, o, do = (np.asarray(t, dtype=np.float64) for t in (q, k, v, o, do))
+    lse = np.asarray(lse, dtype=np.float64)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if key_len is None:
+        key_len = [Nk] * B
+    key_len = [int(x) for x in np.asarray(key_len).reshape(-1)]
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    bounds = (np.zeros_like(v), np.zeros_like(q), np.zeros_like(k)) if parts else None
+    kidx, qidx = np.arange(Nk), np.arange(Nq)
+    for b in range(B):
+        lim = min(max(key_len[b], 0), Nk)
+        vis = np.broadcast_to(kidx[None, :] < lim, (Nq, Nk))
+        if causal:
+            vis = vis & (kidx[None, :] <= qidx[:, None] + (Nk - Nq))
+        for h in range(H):
+            s = scale * (q[b, h] @ k[b, h].T)
+            live = np.isfinite(lse[b, h])[:, None] & vis
+            with np.errstate(invalid="ignore", over="ignore"):
+                p = np.where(live, np.exp(np.where(live, s, 0.0) - np.where(
+                    np.isfinite(lse[b, h]), lse[b, h], 0.0)[:, None]), 0.0)
+            dv[b, h] = p.T @ do[b, h]
+            dp = do[b, h] @ v[b, h].T
+            D = np.sum(do[b, h] * o[b, h], axis=1)
+            ds = p * (dp - D[:, None])
+            dq[b, h] = scale * (ds @ k[b, h])
+            dk[b, h] = scale * (ds.T @ q[b, h])
+            if parts:
+                bounds[0][b, h] = np.abs(p).T @ np.abs(do[b, h])
+                bounds[1][b, h] = scale * (np.abs(ds) @ np.abs(k[b, h]))
+                bounds[2][b, h] = scale * (np.abs(ds).T @ np.abs(q[b, h]))
+    if parts:
+        return dq, dk, dv, bounds
+    return dq, dk, dv
+
+
 def attention_bruteforce(q, k, v, scale, causal=False, key_len=None):
     """Attention by explicit loops and exactly rounded sums (tiny inputs only).
 

@@ -402,3 +402,88 @@ def test_planted_topk_bugs_are_caught():
     wrong_norm = np.exp(x[0][bi]) / np.exp(x[0][bi]).sum()
     assert not np.allclose(wrong_norm, bp, rtol=1e-3)
     assert np.allclose(prob[0], bp, rtol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# Backward ([P3] "From weights to outputs": lse rebuilds the weights).
+
+
+def _loss_grads_fd(q, k, v, do, scale, causal, key_len, eps=1e-6):
+    """Central differences of sum(dO * O) through the forward definition."""
+    def loss(qq, kk, vv):
+        o, _ = O.attention_ref(qq, kk, vv, scale, causal, key_len)
+        return float(np.sum(do * o))
+
+    grads = []
+    for which in range(3):
+        base = [q, k, v][which]
+        g = np.zeros_like(base)
+        it = np.nditer(base, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            args_p = [q.copy(), k.copy(), v.copy()]
+            args_m = [q.copy(), k.copy(), v.copy()]
+            args_p[which][idx] += eps
+            args_m[which][idx] -= eps
+            g[idx] = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+        grads.append(g)
+    return grads
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape,key_len", [((1, 1, 5, 5, 4), None), ((2, 1, 4, 6, 3), [6, 2]),
+                                           ((1, 2, 6, 3, 4), [3]), ((1, 1, 3, 1, 2), None)])
+def test_backward_matches_finite_differences(shape, key_len, causal):
+    B, H, Nq, Nk, d = shape
+    rng = np.random.default_rng(40 + Nq + 7 * causal)
+    q, k, v = (rng.standard_normal(s) for s in ((B, H, Nq, d), (B, H, Nk, d), (B, H, Nk, d)))
+    do = rng.standard_normal((B, H, Nq, d))
+    o, lse = O.attention_ref(q, k, v, 0.7, causal, key_len)
+    dq, dk, dv = O.attention_bwd_ref(q, k, v, o, lse, do, 0.7, causal, key_len)
+    fq, fk, fv = _loss_grads_fd(q, k, v, do, 0.7, causal, key_len)
+    for got, want in ((dq, fq), (dk, fk), (dv, fv)):
+        assert np.allclose(got, want, rtol=1e-6, atol=1e-7)
+
+
+def test_backward_matches_autograd_of_the_definition():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(41)
+    B, H, N, d = 2, 2, 37, 8
+    q, k, v, do = (rng.standard_normal((B, H, N, d)) for _ in range(4))
+    kl = [29, 37]
+    tq, tk, tv = (torch.tensor(t, requires_grad=True) for t in (q, k, v))
+    s = 0.35 * tq @ tk.transpose(-1, -2)
+    j = torch.arange(N)
+    mask = (j[None, :] <= j[:, None])[None, None] & (j[None, None, None, :] < torch.tensor(kl)[:, None, None, None])
+    s = s.masked_fill(~mask, float("-inf"))
+    out = torch.softmax(s, dim=-1) @ tv
+    out.backward(torch.tensor(do))
+    o, lse = O.attention_ref(q, k, v, 0.35, True, kl)
+    dq, dk, dv = O.attention_bwd_ref(q, k, v, o, lse, do, 0.35, True, kl)
+    assert np.allclose(dq, tq.grad.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.allclose(dk, tk.grad.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.allclose(dv, tv.grad.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_backward_rows_without_keys_and_planted_bugs():
+    rng = np.random.default_rng(42)
+    q, k, v, do = (rng.standard_normal((1, 1, 4, 3)) for _ in range(4))
+    # key_len 0: every weight is 0, so every gradient is 0
+    o, lse = O.attention_ref(q, k, v, 0.5, False, [0])
+    assert np.all(np.isneginf(lse))
+    for g in O.attention_bwd_ref(q, k, v, o, lse, do, 0.5, False, [0]):
+        assert np.all(g == 0)
+    # plausible slips fail the finite-difference pin
+    o, lse = O.attention_ref(q, k, v, 0.5, True)
+    fq, fk, fv = _loss_grads_fd(q, k, v, do, 0.5, True, None)
+    s = 0.5 * q[0, 0] @ k[0, 0].T
+    s = np.where(np.arange(4)[None] <= np.arange(4)[:, None], s, -np.inf)
+    p = np.exp(s - lse[0, 0][:, None])
+    dp = do[0, 0] @ v[0, 0].T
+    D = np.sum(do[0, 0] * o[0, 0], axis=1)
+    right = 0.5 * (p * (dp - D[:, None])) @ k[0, 0]
+    assert np.allclose(right, fq[0, 0], rtol=1e-6, atol=1e-7)
+    assert not np.allclose(0.5 * (p * dp) @ k[0, 0], fq[0, 0], rtol=1e-3)        # D dropped
+    assert not np.allclose((p * (dp - D[:, None])) @ k[0, 0], fq[0, 0], rtol=1e-3)  # scale dropped
+    assert not np.allclose(0.5 * (p * (dp - D[:, None])).T @ k[0, 0], fq[0, 0], rtol=1e-3)  # dS^T
+    assert not np.allclose(p @ do[0, 0], fv[0, 0], rtol=1e-3)                       # P not P^T
