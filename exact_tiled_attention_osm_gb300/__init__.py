@@ -37,6 +37,9 @@ SIGNATURES = {
     "osm_softmax_topk": (_I, [_P, _I64, _I64, _I, _P, _P, _P]),
     "osm_attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P]),
     "osm_attn_fwd_bounded": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _F, _P]),
+    "osm_attn_bwd_workspace_bytes": (_SZ, [_I, _I, _I]),
+    "osm_attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P,
+                          _SZ, _P]),
     "osm_attn_decode_splitkv_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "osm_attn_decode_splitkv": (_I, [_I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _I, _P, _SZ, _P]),
     "osm_attn_decode_splitkv_noalloc": (_I, [_I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _I, _P]),
@@ -178,6 +181,38 @@ def attn_fwd(q, k, v, scale=None, causal=False, key_len=None, out=None, lse=None
                                             float(score_bound), _stream(q)),
                    "osm_attn_fwd_bounded")
     return o, lse_t
+
+
+def attn_bwd(q, k, v, o, lse, dout, scale=None, causal=False, key_len=None, workspace=None):
+    """Gradients of attention.  q, o, dout [B,H,Nq,d]; k, v [B,H,Nk,d] bf16 CUDA;
+    lse [B,H,Nq] fp32 (from attn_fwd).  Returns (dq, dk, dv), bf16."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
+        _need(t, n, torch.bfloat16, q.device)
+    _need(lse, "lse", torch.float32, q.device)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if k.shape != (B, H, Nk, d) or v.shape != k.shape or o.shape != q.shape \
+            or dout.shape != q.shape or tuple(lse.shape) != (B, H, Nq):
+        raise ValueError("shapes: q, o, dout [B,H,Nq,d]; k, v [B,H,Nk,d]; lse [B,H,Nq]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    lib = load_library()
+    need = int(lib.osm_attn_bwd_workspace_bytes(B, H, Nq))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _need(workspace, "workspace", torch.uint8, q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    kl = 0
+    if key_len is not None:
+        _need(key_len, "key_len", torch.int32, q.device)
+        kl = key_len.data_ptr()
+    with torch.cuda.device(q.device):
+        _check(lib.osm_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                dv.data_ptr(), B, H, Nq, Nk, d, float(scale), int(bool(causal)),
+                                kl, workspace.data_ptr(), workspace.numel(), _stream(q)),
+               "osm_attn_bwd")
+    return dq, dk, dv
 
 
 def decode_workspace_bytes(B: int, H: int, d: int, num_splits: int) -> int:

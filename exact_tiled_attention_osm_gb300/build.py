@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libosm.so")
 
-SOURCES = ["api.cu", "attn_fwd.cu", "softmax_rows.cu", "softmax_topk.cu", "decode.cu"]
+SOURCES = ["api.cu", "attn_fwd.cu", "attn_bwd.cu", "softmax_rows.cu", "softmax_topk.cu", "decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
           "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -3,6 +3,7 @@
 // launch on the caller's stream.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <limits>
 #include <cstdint>
@@ -95,6 +96,43 @@ osm_status osm_attn_fwd_bounded(const void* q, const void* k, const void* v, voi
   if (!std::isfinite(score_bound) || std::fabs(score_bound) > 1e30f) return OSM_ERR_INVALID_VALUE;
   return attn_fwd_checked(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, key_len, score_bound,
                           stream);
+}
+
+size_t osm_attn_bwd_workspace_bytes(int B, int H, int Nq) {
+  if (B < 0 || H < 0 || Nq < 0) return 0;
+  return osm::attn_bwd_workspace_bytes(B, H, Nq);
+}
+
+osm_status osm_attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                        int H, int Nq, int Nk, int d, float scale, int causal,
+                        const int32_t* key_len, void* workspace, size_t workspace_bytes,
+                        osm_stream_t stream) {
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return OSM_ERR_INVALID_VALUE;
+  if (causal != 0 && causal != 1) return OSM_ERR_INVALID_VALUE;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return OSM_ERR_INVALID_VALUE;
+  if (d != 128) return (d > 0) ? OSM_ERR_UNSUPPORTED : OSM_ERR_INVALID_VALUE;
+  if (static_cast<int64_t>(B) * H == 0 || (Nq == 0 && Nk == 0)) return OSM_OK;
+  if (Nq > 0 && (!q || !o || !lse || !dout || !dq)) return OSM_ERR_INVALID_VALUE;
+  if (Nk > 0 && (!k || !v || !dk || !dv)) return OSM_ERR_INVALID_VALUE;
+  if ((q && !aligned16(q)) || (k && !aligned16(k)) || (v && !aligned16(v)) ||
+      (o && !aligned16(o)) || (dout && !aligned16(dout)) || (dq && !aligned16(dq)) ||
+      (dk && !aligned16(dk)) || (dv && !aligned16(dv)) || (lse && !aligned4(lse)))
+    return OSM_ERR_INVALID_VALUE;
+  if (key_len && !aligned4(key_len)) return OSM_ERR_INVALID_VALUE;
+  if (Nq > 0) {
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+      return OSM_ERR_INVALID_VALUE;
+    if (workspace_bytes < osm::attn_bwd_workspace_bytes(B, H, Nq)) return OSM_ERR_INVALID_VALUE;
+  }
+  const int64_t tiles = static_cast<int64_t>(B) * H * ((std::max(Nq, Nk) + 127) / 128);
+  if (tiles > 0x7fffffffLL) return OSM_ERR_UNSUPPORTED;
+  bool tmap_ok = true;
+  cudaError_t e = osm::launch_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, scale,
+                                       causal, key_len, workspace,
+                                       reinterpret_cast<cudaStream_t>(stream), &tmap_ok);
+  if (!tmap_ok) return OSM_ERR_UNSUPPORTED;
+  return from_cuda(e);
 }
 
 size_t osm_attn_decode_splitkv_workspace_bytes(int B, int H, int d, int num_splits) {
@@ -201,6 +239,10 @@ osm_status osm_device_status(osm_stream_t stream, uint32_t* word) {
   *word = 0;
   cudaError_t e = osm::read_and_clear_device_error(reinterpret_cast<cudaStream_t>(stream), word);
   if (e != cudaSuccess) return OSM_ERR_CUDA;
+  uint32_t wb = 0;  // the backward kernels keep their own word
+  e = osm::read_and_clear_bwd_error(&wb);
+  if (e != cudaSuccess) return OSM_ERR_CUDA;
+  if (*word == 0) *word = wb;
   return *word ? OSM_ERR_TIMEOUT : OSM_OK;
 }
 

@@ -1,0 +1,717 @@
+// attn_bwd.cu — exact softmax attention backward on sm_103a tensor cores.
+//
+// "Online softmax" (zerotofrontier.app), "From weights to outputs": the
+// log-sum-exp kept by the forward pass is all the backward pass needs to
+// rebuild the weights, y_j = exp(s_j - lse).  With s = scale * q.k,
+// P = exp(s - lse) (0 where masked), dO the gradient of the output O:
+//   dV = P^T dO,  dP = dO V^T,  D_i = sum_c dO_ic O_ic,
+//   dS = P * (dP - D)  (elementwise, D broadcast along each row),
+//   dQ = scale * dS K,  dK = scale * dS^T Q.
+// The score and weight matrices are rebuilt tile by tile and never stored.
+//
+// Three kernels:
+//   bwd_delta_kernel  D = rowsum(dO * O), fp32 (HBM-bound).
+//   bwd_dq_kernel     one CTA per (b, h, 128-query tile); streams the visible
+//                     K/V tiles.  S = Q K^T and dP = dO V^T into TMEM; one
+//                     thread per query row forms P and dS (its lse and D stay
+//                     in registers) and writes dS as bf16 over the S columns;
+//                     dQ += dS K with dS read straight from TMEM.
+//   bwd_dkdv_kernel   one CTA per (b, h, 128-key tile); streams the query
+//                     tiles that see it.  S^T = K Q^T and dP^T = V dO^T into
+//                     TMEM; one thread per key row forms P^T and dS^T (lse and
+//                     D per column from shared memory) and writes both as bf16
+//                     over S^T and dP^T; dV += P^T dO and dK += dS^T Q read
+//                     them straight from TMEM.
+// dQ and dK/dV are separate so that no partial sum crosses CTAs (no atomics);
+// the price is S and dP formed twice (7 instead of 5 matrix products).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tmap.h"
+
+namespace osm {
+namespace bwd {
+
+using namespace ptx;
+
+constexpr int kHeadDim = 128;
+constexpr int kTile = 128;   // rows of every tile (query or key)
+constexpr int kSlots = 4;    // streamed 32 KB tiles in flight
+constexpr uint32_t kTileBytes = kTile * kHeadDim * 2;  // 32768
+constexpr uint32_t kBoxBytes = 128 * 64 * 2;           // one TMA box: 64 columns x 128 rows
+constexpr int kThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kNegInf = -__builtin_huge_valf();
+constexpr float kPosInf = __builtin_huge_valf();
+
+// shared memory: two resident tiles, then the ring
+constexpr uint32_t kSmemRes = 0;
+constexpr uint32_t kSmemRing = 2 * kTileBytes;
+constexpr uint32_t kSmemBar = kSmemRing + kSlots * kTileBytes;
+enum Bar : uint32_t {
+  RES_FULL = 0,
+  RING_FULL = 1,                 // [kSlots]
+  RING_EMPTY = 1 + kSlots,       // [kSlots]
+  S_FULL = 1 + 2 * kSlots,
+  P_FULL = S_FULL + 1,
+  O_FULL = P_FULL + 1,
+  DRAIN = O_FULL + 1,
+  NUM_BARS
+};
+constexpr uint32_t kSmemTmemSlot = kSmemBar + 8 * NUM_BARS;
+constexpr uint32_t kSmemAbort = kSmemTmemSlot + 4;
+// per softmax warp: [2 buffers][lse2 | D][128 columns] floats
+constexpr uint32_t kSmemCol = (kSmemAbort + 4 + 15) / 16 * 16;
+constexpr uint32_t kColFloats = 2 * 2 * kTile;
+constexpr uint32_t kSmemBytes = kSmemCol + 4 * kColFloats * 4 + 1024;
+
+constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemAcc0 = 256, kTmemAcc1 = 384;
+
+constexpr uint32_t kIdescKK = idesc_bf16_f32(128, 128, false);  // both operands K-major
+constexpr uint32_t kIdescKMN = idesc_bf16_f32(128, 128, true);  // B MN-major
+
+constexpr unsigned kSiteQ = 0x02000000u;   // error-word sites of the dQ kernel
+constexpr unsigned kSiteK = 0x03000000u;   // ... and of the dK/dV kernel
+
+struct Params {
+  int B, H, Nq, Nk;
+  int causal;
+  int n_qt, n_kt;     // query / key tiles per head
+  float scale, scale_log2;
+  const int32_t* key_len;
+  const float* lse;   // [B*H*Nq] natural log
+  const float* delta; // [B*H*Nq]
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  unsigned int* err;
+};
+
+__device__ __forceinline__ int key_len_of(const Params& p, int b) {
+  int L = p.key_len ? p.key_len[b] : p.Nk;
+  return L < 0 ? 0 : (L > p.Nk ? p.Nk : L);
+}
+
+// 16-byte global stores of one 128-column bf16 row from four 32-column TMEM chunks
+__device__ __forceinline__ void store_row_bf16(uint32_t t_acc, float mul, __nv_bfloat16* dst,
+                                               bool ok) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t r[32];
+    tmem_ld_x32(t_acc + 32 * c, r);
+    if (ok) {
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(r[2 * e]) * mul,
+                                                  __uint_as_float(r[2 * e + 1]) * mul);
+        pk[e] = *reinterpret_cast<uint32_t*>(&h2);
+      }
+      uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+    }
+  }
+}
+
+__device__ __forceinline__ void zero_row_bf16(__nv_bfloat16* dst) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int e = 0; e < kHeadDim / 8; ++e) d4[e] = make_uint4(0, 0, 0, 0);
+}
+
+__device__ unsigned int g_bwd_err;
+
+// ------------------------------------------------------------------ D
+__global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
+                                                        const __nv_bfloat16* __restrict__ dout,
+                                                        float* __restrict__ delta, int64_t rows) {
+  // 16 lanes per row, 8 columns (one 16-byte load of each tensor) per lane
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t row = t >> 4;
+  const int sl = threadIdx.x & 15;
+  float acc = 0.f;
+  if (row < rows) {
+    const uint4 a = reinterpret_cast<const uint4*>(o + row * kHeadDim)[sl];
+    const uint4 g = reinterpret_cast<const uint4*>(dout + row * kHeadDim)[sl];
+    const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wg[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc = fmaf(__uint_as_float(wa[i] << 16), __uint_as_float(wg[i] << 16), acc);
+      acc = fmaf(__uint_as_float(wa[i] & 0xffff0000u), __uint_as_float(wg[i] & 0xffff0000u), acc);
+    }
+  }
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && sl == 0) delta[row] = acc;
+}
+
+// ------------------------------------------------------------------ dQ
+// Item = (bh, query tile); causal items longest first.
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sQ = sbase + kSmemRes, sDO = sQ + kTileBytes, sRing = sbase + kSmemRing;
+  auto bar = [&](uint32_t i) { return sbase + kSmemBar + 8 * i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSmemTmemSlot);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int within = blockIdx.x % p.n_qt;
+  const int bh = blockIdx.x / p.n_qt;
+  const int qt = p.causal ? (p.n_qt - 1 - within) : within;
+  const int q0 = qt * kTile;
+  const int b = bh / p.H;
+  const int L = key_len_of(p, b);
+  int kend = L;
+  if (p.causal) kend = min(L, max(0, min(q0 + kTile, p.Nq) + (p.Nk - p.Nq)));
+  const int n_kv = (kend + kTile - 1) / kTile;
+
+  if (n_kv == 0) {  // no visible key for any row of the tile: dQ = 0
+    if (warp >= 4) {
+      const int row = q0 + 32 * (warp - 4) + lane;
+      if (row < p.Nq) zero_row_bf16(p.dq + (static_cast<int64_t>(bh) * p.Nq + row) * kHeadDim);
+    }
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(RES_FULL), 1);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(bar(RING_FULL + s), 1);
+      mbar_init(bar(RING_EMPTY + s), 1);
+    }
+    mbar_init(bar(S_FULL), 1);
+    mbar_init(bar(P_FULL), 4);
+    mbar_init(bar(O_FULL), 1);
+    mbar_init(bar(DRAIN), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  auto wait_one = [&](uint32_t bb, uint32_t parity, unsigned site) -> bool {
+    return wait_bounded(bb, parity, abort_flag, p.err, site);
+  };
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------- TMA producer
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_do);
+    mbar_arrive_expect_tx(bar(RES_FULL), 2 * kTileBytes);
+    for (int c = 0; c < 2; ++c) {
+      tma_load_3d(sQ + c * kBoxBytes, &tm_q, bar(RES_FULL), c * 64, q0, bh);
+      tma_load_3d(sDO + c * kBoxBytes, &tm_do, bar(RES_FULL), c * 64, q0, bh);
+    }
+    uint32_t slot = 0, ph = 0, fill_mask = 0, fill_ph = 0;
+    bool ok = true;
+    for (int j = 0; ok && j < n_kv; ++j) {
+      for (int kv = 0; kv < 2; ++kv) {  // K_j then V_j
+        if (!(ok = wait_one(bar(RING_EMPTY + slot), ph ^ 1, kSiteQ | 1))) break;
+        mbar_arrive_expect_tx(bar(RING_FULL + slot), kTileBytes);
+        const CUtensorMap* tm = kv ? &tm_v : &tm_k;
+        for (int c = 0; c < 2; ++c)
+          tma_load_3d(sRing + slot * kTileBytes + c * kBoxBytes, tm, bar(RING_FULL + slot), c * 64,
+                      j * kTile, bh);
+        fill_mask |= 1u << slot;
+        fill_ph = (fill_ph & ~(1u << slot)) | (ph << slot);
+        if (++slot == kSlots) { slot = 0; ph ^= 1; }
+      }
+    }
+    if (!ok) {  // let every copy this thread started land before the CTA exits
+      for (int s = 0; s < kSlots; ++s)
+        if (fill_mask >> s & 1u) wait_drain(bar(RING_FULL + s), fill_ph >> s & 1u, 200000000ull);
+      wait_drain(bar(RES_FULL), 0, 200000000ull);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------- MMA issuer
+    const uint64_t dKm = sdesc_sw128(0, 16, 1024);      // K-major template
+    const uint64_t dMN = sdesc_sw128(0, 16384, 1024);   // MN-major template
+    bool ok = wait_one(bar(RES_FULL), 0, kSiteQ | 2);
+    uint32_t slot = 0, ph = 0, pf_ph = 0;
+    uint32_t k_prev = 0;  // ring slot of K_{j-1}
+    if (ok) {
+      tc_fence_after();
+      const uint64_t qdesc = dKm + (sQ >> 4), dodesc = dKm + (sDO >> 4);
+      // dQ += dS_{j-1} K_{j-1}, once the softmax warps have written dS
+      auto issue_dq = [&](int jj) -> bool {
+        if (!wait_one(bar(P_FULL), pf_ph, kSiteQ | 3)) return false;
+        pf_ph ^= 1;
+        tc_fence_after();
+        const uint64_t kdesc = dMN + ((sRing + k_prev * kTileBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tbase + kTmemAcc0, tbase + kTmemS + kk * 8, kdesc + ((kk * 2048) >> 4), kIdescKMN,
+                 (jj > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(RING_EMPTY + k_prev));  // K_{j-1} is free after this product
+        return true;
+      };
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const uint32_t ks = slot;
+        if (!(ok = wait_one(bar(RING_FULL + ks), ph, kSiteQ | 4))) break;
+        if (++slot == kSlots) { slot = 0; ph ^= 1; }
+        const uint32_t vs = slot;
+        if (!(ok = wait_one(bar(RING_FULL + vs), ph, kSiteQ | 4))) break;
+        if (++slot == kSlots) { slot = 0; ph ^= 1; }
+        if (j > 0 && !(ok = issue_dq(j - 1))) break;
+        tc_fence_after();
+        const uint64_t kdesc = dKm + ((sRing + ks * kTileBytes) >> 4);
+        const uint64_t vdesc = dKm + ((sRing + vs * kTileBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+          mma_ss(tbase + kTmemS, qdesc + off, kdesc + off, kIdescKK, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+          mma_ss(tbase + kTmemDP, dodesc + off, vdesc + off, kIdescKK, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(S_FULL));
+        mma_commit(bar(RING_EMPTY + vs));  // V_j is used by dP_j only
+        k_prev = ks;
+      }
+      if (ok && (ok = issue_dq(n_kv - 1))) mma_commit(bar(O_FULL));
+    }
+    if (!ok) {  // wait for every MMA already issued before TMEM is released
+      mma_commit(bar(DRAIN));
+      wait_drain(bar(DRAIN), 0, 200000000ull);
+    }
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------- P and dS
+    const int wq = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * wq) << 16;
+    const uint32_t tS = tbase + lane_off + kTmemS, tDP = tbase + lane_off + kTmemDP;
+    const int row = q0 + 32 * wq + lane;
+    const bool row_ok = row < p.Nq;
+    const int64_t grow = static_cast<int64_t>(bh) * p.Nq + (row_ok ? row : 0);
+    float lse2 = row_ok ? p.lse[grow] * kLog2e : kPosInf;
+    if (!(lse2 > kNegInf)) lse2 = kPosInf;  // a row with no visible key: every P is 0
+    const float dlt = row_ok ? p.delta[grow] : 0.f;
+    int limit = L;
+    if (p.causal) limit = min(limit, row + 1 + (p.Nk - p.Nq));
+    const float sl2 = p.scale_log2;
+    uint32_t sf_ph = 0;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      ok = __all_sync(0xffffffffu, wait_one(bar(S_FULL), sf_ph, kSiteQ | 5));
+      if (!ok) break;
+      sf_ph ^= 1;
+      tc_fence_after();
+      const int k0 = j * kTile;
+      const bool masked_tile = __any_sync(0xffffffffu, k0 + kTile > limit);
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t s[32], dp[32], pk[16];
+        tmem_ld_x32(tS + 32 * ch, s);
+        tmem_ld_x32(tDP + 32 * ch, dp);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float p0 = ex2(fmaf(__uint_as_float(s[e]), sl2, -lse2));
+          float p1 = ex2(fmaf(__uint_as_float(s[e + 1]), sl2, -lse2));
+          if (masked_tile) {
+            if (k0 + 32 * ch + e >= limit) p0 = 0.f;
+            if (k0 + 32 * ch + e + 1 >= limit) p1 = 0.f;
+          }
+          const float g0 = p0 * (__uint_as_float(dp[e]) - dlt);
+          const float g1 = p1 * (__uint_as_float(dp[e + 1]) - dlt);
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(g0, g1);
+          pk[e >> 1] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+        tmem_st_x16_nowait(tS + 16 * ch, pk);  // dS over S columns already read
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(P_FULL));
+    }
+    if (ok) ok = __all_sync(0xffffffffu, wait_one(bar(O_FULL), 0, kSiteQ | 6));
+    if (ok) {
+      tc_fence_after();
+      store_row_bf16(tbase + lane_off + kTmemAcc0, p.scale,
+                     p.dq + (static_cast<int64_t>(bh) * p.Nq + row) * kHeadDim, row_ok);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tbase, 512);
+}
+
+// ------------------------------------------------------------------ dK, dV
+// Item = (bh, key tile); causal items longest first (early key tiles are
+// seen by the most query tiles).
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_do, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sK = sbase + kSmemRes, sV = sK + kTileBytes, sRing = sbase + kSmemRing;
+  auto bar = [&](uint32_t i) { return sbase + kSmemBar + 8 * i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSmemTmemSlot);
+  float* col = reinterpret_cast<float*>(smem + kSmemCol);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int kt = blockIdx.x % p.n_kt;  // causal: key tile 0 first (it has the most work)
+  const int bh = blockIdx.x / p.n_kt;
+  const int k0 = kt * kTile;
+  const int b = bh / p.H;
+  const int L = key_len_of(p, b);
+  const int off = p.Nk - p.Nq;
+  int qt_first = 0;
+  if (p.causal) qt_first = max(0, k0 - off) / kTile;
+  const int n_q = (k0 < L && (!p.causal || k0 - off < p.Nq)) ? p.n_qt - qt_first : 0;
+
+  if (n_q == 0) {  // every key of the tile is invisible to every query: dK = dV = 0
+    if (warp >= 4) {
+      const int key = k0 + 32 * (warp - 4) + lane;
+      if (key < p.Nk) {
+        const int64_t g = (static_cast<int64_t>(bh) * p.Nk + key) * kHeadDim;
+        zero_row_bf16(p.dk + g);
+        zero_row_bf16(p.dv + g);
+      }
+    }
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(RES_FULL), 1);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(bar(RING_FULL + s), 1);
+      mbar_init(bar(RING_EMPTY + s), 1);
+    }
+    mbar_init(bar(S_FULL), 1);
+    mbar_init(bar(P_FULL), 4);
+    mbar_init(bar(O_FULL), 1);
+    mbar_init(bar(DRAIN), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  auto wait_one = [&](uint32_t bb, uint32_t parity, unsigned site) -> bool {
+    return wait_bounded(bb, parity, abort_flag, p.err, site);
+  };
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------- TMA producer
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_do);
+    mbar_arrive_expect_tx(bar(RES_FULL), 2 * kTileBytes);
+    for (int c = 0; c < 2; ++c) {
+      tma_load_3d(sK + c * kBoxBytes, &tm_k, bar(RES_FULL), c * 64, k0, bh);
+      tma_load_3d(sV + c * kBoxBytes, &tm_v, bar(RES_FULL), c * 64, k0, bh);
+    }
+    uint32_t slot = 0, ph = 0, fill_mask = 0, fill_ph = 0;
+    bool ok = true;
+    for (int i = 0; ok && i < n_q; ++i) {
+      const int qrow = (qt_first + i) * kTile;
+      for (int t = 0; t < 2; ++t) {  // Q_i then dO_i
+        if (!(ok = wait_one(bar(RING_EMPTY + slot), ph ^ 1, kSiteK | 1))) break;
+        mbar_arrive_expect_tx(bar(RING_FULL + slot), kTileBytes);
+        const CUtensorMap* tm = t ? &tm_do : &tm_q;
+        for (int c = 0; c < 2; ++c)
+          tma_load_3d(sRing + slot * kTileBytes + c * kBoxBytes, tm, bar(RING_FULL + slot), c * 64,
+                      qrow, bh);
+        fill_mask |= 1u << slot;
+        fill_ph = (fill_ph & ~(1u << slot)) | (ph << slot);
+        if (++slot == kSlots) { slot = 0; ph ^= 1; }
+      }
+    }
+    if (!ok) {
+      for (int s = 0; s < kSlots; ++s)
+        if (fill_mask >> s & 1u) wait_drain(bar(RING_FULL + s), fill_ph >> s & 1u, 200000000ull);
+      wait_drain(bar(RES_FULL), 0, 200000000ull);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------- MMA issuer
+    const uint64_t dKm = sdesc_sw128(0, 16, 1024);
+    const uint64_t dMN = sdesc_sw128(0, 16384, 1024);
+    bool ok = wait_one(bar(RES_FULL), 0, kSiteK | 2);
+    uint32_t slot = 0, ph = 0, pf_ph = 0;
+    uint32_t q_prev = 0, do_prev = 0;
+    if (ok) {
+      tc_fence_after();
+      const uint64_t kdesc = dKm + (sK >> 4), vdesc = dKm + (sV >> 4);
+      // dV += P^T_{i-1} dO_{i-1}, dK += dS^T_{i-1} Q_{i-1}
+      auto issue_acc = [&](int ii) -> bool {
+        if (!wait_one(bar(P_FULL), pf_ph, kSiteK | 3)) return false;
+        pf_ph ^= 1;
+        tc_fence_after();
+        const uint64_t dod = dMN + ((sRing + do_prev * kTileBytes) >> 4);
+        const uint64_t qd = dMN + ((sRing + q_prev * kTileBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tbase + kTmemAcc0, tbase + kTmemS + kk * 8, dod + ((kk * 2048) >> 4), kIdescKMN,
+                 (ii > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tbase + kTmemAcc1, tbase + kTmemDP + kk * 8, qd + ((kk * 2048) >> 4), kIdescKMN,
+                 (ii > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(RING_EMPTY + q_prev));
+        mma_commit(bar(RING_EMPTY + do_prev));
+        return true;
+      };
+      for (int i = 0; ok && i < n_q; ++i) {
+        const uint32_t qs = slot;
+        if (!(ok = wait_one(bar(RING_FULL + qs), ph, kSiteK | 4))) break;
+        if (++slot == kSlots) { slot = 0; ph ^= 1; }
+        const uint32_t ds = slot;
+        if (!(ok = wait_one(bar(RING_FULL + ds), ph, kSiteK | 4))) break;
+        if (++slot == kSlots) { slot = 0; ph ^= 1; }
+        if (i > 0 && !(ok = issue_acc(i - 1))) break;
+        tc_fence_after();
+        const uint64_t qdesc = dKm + ((sRing + qs * kTileBytes) >> 4);
+        const uint64_t dodesc = dKm + ((sRing + ds * kTileBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+          const uint32_t o16 = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+          mma_ss(tbase + kTmemS, kdesc + o16, qdesc + o16, kIdescKK, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+          const uint32_t o16 = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+          mma_ss(tbase + kTmemDP, vdesc + o16, dodesc + o16, kIdescKK, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(S_FULL));
+        q_prev = qs;
+        do_prev = ds;
+      }
+      if (ok && (ok = issue_acc(n_q - 1))) mma_commit(bar(O_FULL));
+    }
+    if (!ok) {
+      mma_commit(bar(DRAIN));
+      wait_drain(bar(DRAIN), 0, 200000000ull);
+    }
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------- P^T and dS^T
+    const int wq = warp & 3;
+    const int tid = threadIdx.x - 128;  // 0..127: this thread's key row
+    const uint32_t lane_off = static_cast<uint32_t>(32 * wq) << 16;
+    const uint32_t tS = tbase + lane_off + kTmemS, tDP = tbase + lane_off + kTmemDP;
+    const int key = k0 + tid;
+    const bool key_ok = key < L;  // keys past the valid length see no query
+    const float sl2 = p.scale_log2;
+    const int64_t hrow = static_cast<int64_t>(bh) * p.Nq;
+    // Per-column lse (base 2) and D of query tile i.  Every warp stages its
+    // own copy in shared memory (lane l loads columns 4l..4l+3), so only
+    // __syncwarp is needed; the next tile's values load while this one runs.
+    float* colw = col + wq * kColFloats;
+    auto col_vals = [&](int i, float (&l2)[4], float (&dd)[4]) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int q = (qt_first + i) * kTile + 4 * lane + u;
+        if (q < p.Nq) {
+          l2[u] = p.lse[hrow + q] * kLog2e;
+          if (!(l2[u] > kNegInf)) l2[u] = kPosInf;  // a query with no visible key: P = 0
+          dd[u] = p.delta[hrow + q];
+        } else {
+          l2[u] = kPosInf;
+          dd[u] = 0.f;
+        }
+      }
+    };
+    float nl2[4], nd[4];
+    col_vals(0, nl2, nd);
+    uint32_t sf_ph = 0;
+    bool ok = true;
+    for (int i = 0; i < n_q; ++i) {
+      float* cl = colw + (i & 1) * 2 * kTile;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        cl[4 * lane + u] = nl2[u];
+        cl[kTile + 4 * lane + u] = nd[u];
+      }
+      __syncwarp();
+      if (i + 1 < n_q) col_vals(i + 1, nl2, nd);
+      ok = __all_sync(0xffffffffu, wait_one(bar(S_FULL), sf_ph, kSiteK | 5));
+      if (!ok) break;
+      sf_ph ^= 1;
+      tc_fence_after();
+      const int qb = (qt_first + i) * kTile;
+      // the tile needs the causal mask when some (key, query) pair is hidden
+      const bool masked_tile = p.causal && __any_sync(0xffffffffu, key > qb + off);
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t s[32], dp[32], pk[16], gk[16];
+        tmem_ld_x32(tS + 32 * ch, s);
+        tmem_ld_x32(tDP + 32 * ch, dp);
+        const float4* cl4 = reinterpret_cast<const float4*>(cl + 32 * ch);
+        const float4* cd4 = reinterpret_cast<const float4*>(cl + kTile + 32 * ch);
+#pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 l4 = cl4[e4], d4 = cd4[e4];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pr[4], gr[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int e = 4 * e4 + u;
+            float pe = ex2(fmaf(__uint_as_float(s[e]), sl2, -lv[u]));
+            if (!key_ok) pe = 0.f;
+            if (masked_tile && key > qb + 32 * ch + e + off) pe = 0.f;
+            pr[u] = pe;
+            gr[u] = pe * (__uint_as_float(dp[e]) - dv[u]);
+          }
+          __nv_bfloat162 a0 = __floats2bfloat162_rn(pr[0], pr[1]);
+          __nv_bfloat162 a1 = __floats2bfloat162_rn(pr[2], pr[3]);
+          __nv_bfloat162 g0 = __floats2bfloat162_rn(gr[0], gr[1]);
+          __nv_bfloat162 g1 = __floats2bfloat162_rn(gr[2], gr[3]);
+          pk[2 * e4] = *reinterpret_cast<uint32_t*>(&a0);
+          pk[2 * e4 + 1] = *reinterpret_cast<uint32_t*>(&a1);
+          gk[2 * e4] = *reinterpret_cast<uint32_t*>(&g0);
+          gk[2 * e4 + 1] = *reinterpret_cast<uint32_t*>(&g1);
+        }
+        tmem_st_x16_nowait(tS + 16 * ch, pk);   // P^T over S^T columns already read
+        tmem_st_x16_nowait(tDP + 16 * ch, gk);  // dS^T over dP^T columns already read
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(P_FULL));
+    }
+    if (ok) ok = __all_sync(0xffffffffu, wait_one(bar(O_FULL), 0, kSiteK | 6));
+    if (ok) {
+      tc_fence_after();
+      const bool st_ok = key < p.Nk;
+      const int64_t g = (static_cast<int64_t>(bh) * p.Nk + (st_ok ? key : 0)) * kHeadDim;
+      store_row_bf16(tbase + lane_off + kTmemAcc0, 1.f, p.dv + g, st_ok);
+      store_row_bf16(tbase + lane_off + kTmemAcc1, p.scale, p.dk + g, st_ok);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tbase, 512);
+}
+
+}  // namespace bwd
+
+size_t attn_bwd_workspace_bytes(int B, int H, int Nq) {
+  return ((static_cast<size_t>(B) * H * Nq * 4 + 255) / 256) * 256;
+}
+
+cudaError_t launch_attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                            const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                            int B, int H, int Nq, int Nk, float scale, int causal,
+                            const int32_t* key_len, void* workspace, cudaStream_t s,
+                            bool* tmap_ok) {
+  using namespace bwd;
+  *tmap_ok = true;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  const int64_t qrows = BH * Nq;
+  float* delta = static_cast<float*>(workspace);
+  if (Nq > 0) {
+    bwd_delta_kernel<<<static_cast<unsigned>((qrows * 16 + 255) / 256), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), delta,
+        qrows);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_tmap_bf16_3d(&tq, q, kHeadDim, Nq, BH, 64, kTile) ||
+      !make_tmap_bf16_3d(&tk, k, kHeadDim, Nk, BH, 64, kTile) ||
+      !make_tmap_bf16_3d(&tv, v, kHeadDim, Nk, BH, 64, kTile) ||
+      !make_tmap_bf16_3d(&tdo, dout, kHeadDim, Nq, BH, 64, kTile)) {
+    *tmap_ok = false;
+    return cudaSuccess;
+  }
+  Params p;
+  p.B = B;
+  p.H = H;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.causal = causal ? 1 : 0;
+  p.n_qt = (Nq + kTile - 1) / kTile;
+  p.n_kt = (Nk + kTile - 1) / kTile;
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.key_len = key_len;
+  p.lse = lse;
+  p.delta = delta;
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  void* errp = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&errp, g_bwd_err);
+  if (e != cudaSuccess) return e;
+  p.err = static_cast<unsigned int*>(errp);
+  static unsigned long long attr_done = 0;
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(attr_done & bit)) {
+    e = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_done |= bit;
+  }
+  if (Nk > 0 && Nq > 0) {
+    bwd_dkdv_kernel<<<static_cast<unsigned>(BH * p.n_kt), kThreads, kSmemBytes, s>>>(tq, tk, tv,
+                                                                                   tdo, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  } else if (Nk > 0) {  // no query: dK = dV = 0
+    e = cudaMemsetAsync(dk, 0, static_cast<size_t>(BH) * Nk * kHeadDim * 2, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, static_cast<size_t>(BH) * Nk * kHeadDim * 2, s);
+    if (e != cudaSuccess) return e;
+  }
+  if (Nq > 0) {
+    if (Nk > 0) {
+      bwd_dq_kernel<<<static_cast<unsigned>(BH * p.n_qt), kThreads, kSmemBytes, s>>>(tq, tk, tv,
+                                                                                   tdo, p);
+      e = cudaGetLastError();
+    } else {  // no key: dQ = 0
+      e = cudaMemsetAsync(dq, 0, static_cast<size_t>(BH) * Nq * kHeadDim * 2, s);
+    }
+  }
+  return e;
+}
+
+cudaError_t read_and_clear_bwd_error(uint32_t* word) {
+  unsigned int w = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&w, bwd::g_bwd_err, sizeof(w));
+  if (e != cudaSuccess) return e;
+  if (w != 0) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(bwd::g_bwd_err, &zero, sizeof(zero));
+    if (e != cudaSuccess) return e;
+  }
+  *word = w;
+  return cudaSuccess;
+}
+
+}  // namespace osm

@@ -25,6 +25,15 @@ cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o
                             bool* tmap_ok);
 cudaError_t read_and_clear_device_error(cudaStream_t s, uint32_t* word);
 
+// attn_bwd.cu
+size_t attn_bwd_workspace_bytes(int B, int H, int Nq);
+cudaError_t launch_attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                            const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                            int B, int H, int Nq, int Nk, float scale, int causal,
+                            const int32_t* key_len, void* workspace, cudaStream_t s,
+                            bool* tmap_ok);
+cudaError_t read_and_clear_bwd_error(uint32_t* word);
+
 // decode.cu
 size_t decode_workspace_bytes(int B, int H, int d, int S);
 cudaError_t launch_decode_splitkv(osm_dtype dt, const void* q, const void* k, const void* v,

@@ -154,6 +154,36 @@ osm_status osm_attn_fwd_bounded(const void *q, const void *k, const void *v, voi
                                 osm_stream_t stream);
 
 /*
+ * osm_attn_bwd — gradients of exact softmax attention, BF16 in and out.
+ *
+ * Defines ([P3] "From weights to outputs": the log-sum-exp is all the
+ * backward pass needs to rebuild the weights, y_j = exp(s_j - lse)): with s,
+ * the masks and lse as in osm_attn_fwd, P = exp(s - lse) (0 where masked),
+ * and dO the gradient of O,
+ *   dV = P^T dO,   dP = dO V^T,   D_i = sum_c dO_ic O_ic,
+ *   dS = P * (dP - D_i),   dQ = scale dS K,   dK = scale dS^T Q.
+ * The weights are rebuilt tile by tile from q, k and lse; no score matrix is
+ * stored.  Three launches on `stream`: D (into the workspace), dK and dV (one
+ * CTA per 128-key tile), dQ (one CTA per 128-query tile).
+ *
+ *   q [B, H, Nq, d], k, v [B, H, Nk, d], o and dout [B, H, Nq, d]: bf16, read only
+ *         (o and lse as written by osm_attn_fwd for the same inputs).
+ *   lse   [B, H, Nq] fp32, natural log (-inf for a row with no visible key).
+ *   dq [B, H, Nq, d], dk, dv [B, H, Nk, d]: bf16, written.
+ *   d, scale, causal, key_len: as osm_attn_fwd.  Keys past key_len get
+ *         dK = dV = 0.
+ *   workspace >= osm_attn_bwd_workspace_bytes(B, H, Nq) bytes of device
+ *         memory, 256-byte aligned (holds D, fp32 [B, H, Nq]).
+ *   q, k, v, o, dout, dq, dk, dv 16-byte aligned.
+ */
+size_t osm_attn_bwd_workspace_bytes(int B, int H, int Nq);
+osm_status osm_attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                        const float *lse, const void *dout, void *dq, void *dk, void *dv, int B,
+                        int H, int Nq, int Nk, int d, float scale, int causal,
+                        const int32_t *key_len, void *workspace, size_t workspace_bytes,
+                        osm_stream_t stream);
+
+/*
  * osm_attn_decode_splitkv_workspace_bytes — bytes of device workspace that
  * osm_attn_decode_splitkv needs for these sizes (0 if a size is invalid).
  *

@@ -136,6 +136,34 @@ def test_bounded_attn_validation(lib):
     assert call(5, 0) == osm.OSM_OK                                 # empty: no-op
 
 
+def test_bwd_validation(lib):
+    f = lib.osm_attn_bwd
+    need = lib.osm_attn_bwd_workspace_bytes(1, 1, 128)
+    assert need == 512
+    names = ["q", "k", "v", "o", "lse", "do", "dq", "dk", "dv", "B", "H", "Nq", "Nk", "d",
+             "scale", "causal", "kl", "ws", "wsb", "s"]
+    base = [FAKE] * 9 + [1, 1, 128, 128, 128, 0.088, 0, None, FAKE, need, None]
+
+    def call(**kw):
+        a = list(base)
+        for key, val in kw.items():
+            a[names.index(key)] = val
+        return f(*a)
+
+    assert call(q=None) == osm.OSM_ERR_INVALID_VALUE
+    assert call(do=None) == osm.OSM_ERR_INVALID_VALUE
+    assert call(dk=None) == osm.OSM_ERR_INVALID_VALUE
+    assert call(lse=FAKE + 2) == osm.OSM_ERR_INVALID_VALUE
+    assert call(dq=FAKE + 8) == osm.OSM_ERR_INVALID_VALUE
+    assert call(d=64) == osm.OSM_ERR_UNSUPPORTED
+    assert call(scale=0.0) == osm.OSM_ERR_INVALID_VALUE
+    assert call(causal=3) == osm.OSM_ERR_INVALID_VALUE
+    assert call(ws=None) == osm.OSM_ERR_INVALID_VALUE
+    assert call(ws=FAKE + 16) == osm.OSM_ERR_INVALID_VALUE
+    assert call(wsb=need - 1) == osm.OSM_ERR_INVALID_VALUE
+    assert call(B=0) == osm.OSM_OK                                  # empty: no-op
+
+
 def test_decode_and_merge_validation(lib):
     f = lib.osm_attn_decode_splitkv
     need = osm.decode_workspace_bytes(2, 2, 128, 4)
