@@ -14,6 +14,7 @@ from .ref import (  # noqa: F401
     merge,
     merge_all,
     online_attention_single,
+    online_attention_single_normalised,
     online_ml_trace,
     set_partitions,
     softmax_row_fsum,

@@ -426,6 +426,33 @@ def online_attention_single(q: np.ndarray, k: np.ndarray, v: np.ndarray,
     return acc / l, m + math.log(l)
 
 
+def online_attention_single_normalised(q: np.ndarray, k: np.ndarray, v: np.ndarray,
+                                       scale: float = 1.0,
+                                       block: int = 64) -> Tuple[np.ndarray, float]:
+    """The same stream, keeping the output normalised after every block.
+
+    [P3] "From weights to outputs", the second way to write it (the form of
+    the original FlashAttention): with o = O~ / l held instead of O~, a block
+    step is o_new = (l e^{m - m_new} o + sum_j e^{s_j - m_new} v_j) / l_new,
+    one division per step instead of one at the end.  Both forms are exact;
+    the pages call the per-step division wasted work.  Returns (o, lse).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    m, l = NEG_INF, 0.0
+    o = np.zeros(v.shape[1])
+    for start in range(0, k.shape[0], block):
+        s = scale * (k[start:start + block] @ q)
+        m_new = max(m, float(np.max(s)))
+        shrink = 0.0 if m == NEG_INF else math.exp(m - m_new)
+        w = np.exp(s - m_new)
+        l_new = shrink * l + float(np.sum(w))
+        o = (shrink * l * o + w @ v[start:start + block]) / l_new
+        m, l = m_new, l_new
+    return o, m + math.log(l)
+
+
 # ---------------------------------------------------------------------------
 # Helpers used only by the pin tests.
 # ---------------------------------------------------------------------------

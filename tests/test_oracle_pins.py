@@ -487,3 +487,33 @@ def test_backward_rows_without_keys_and_planted_bugs():
     assert not np.allclose((p * (dp - D[:, None])) @ k[0, 0], fq[0, 0], rtol=1e-3)  # scale dropped
     assert not np.allclose(0.5 * (p * (dp - D[:, None])).T @ k[0, 0], fq[0, 0], rtol=1e-3)  # dS^T
     assert not np.allclose(p @ do[0, 0], fv[0, 0], rtol=1e-3)                       # P not P^T
+
+
+def test_normalised_form_equals_the_unnormalised_one():
+    """[P3] "From weights to outputs": keeping o = O~ / l after every block (the
+    original FlashAttention form) is exact too -- against the definition and
+    the unnormalised stream, for several block sizes, and a planted slip
+    (the old output not weighted by its share l e^{m - m_new} / l_new)."""
+    rng = np.random.default_rng(43)
+    q, k, v = rng.standard_normal(16), rng.standard_normal((300, 16)), rng.standard_normal((300, 16))
+    k[170] *= 6.0                                    # the max jumps mid-stream
+    o_def, lse_def = O.attention_ref(q[None, None, None], k[None, None], v[None, None], 0.4)
+    for block in (1, 7, 64, 300):
+        o_n, lse_n = O.online_attention_single_normalised(q, k, v, 0.4, block)
+        o_u, lse_u = O.online_attention_single(q, k, v, 0.4, block)
+        assert np.allclose(o_n, o_def[0, 0, 0], rtol=1e-13, atol=1e-14)
+        assert np.allclose(o_n, o_u, rtol=1e-13, atol=1e-14)
+        assert lse_n == pytest.approx(lse_def[0, 0, 0], rel=1e-14)
+    m, l, o = NEG_INF_, 0.0, np.zeros(16)
+    for start in range(0, 300, 64):                  # the slip: o_new = o + w V / l_new
+        s = 0.4 * (k[start:start + 64] @ q)
+        m_new = max(m, s.max())
+        shrink = 0.0 if m == NEG_INF_ else np.exp(m - m_new)
+        w = np.exp(s - m_new)
+        l_new = shrink * l + w.sum()
+        o = o + (w @ v[start:start + 64]) / l_new
+        m, l = m_new, l_new
+    assert not np.allclose(o, o_def[0, 0, 0], rtol=1e-3)
+
+
+NEG_INF_ = float("-inf")
