@@ -13,10 +13,14 @@
 //
 // GB300 mapping: one cluster of nct CTAs (256 threads each) per row; CTA r of
 // the cluster streams a contiguous slice of the row with 16-byte loads, four
-// in flight per thread.  Lists merge by k rounds of a warp-wide arg-max over
-// the lanes' list heads; the CTA's lists meet in shared memory and the
-// cluster's in CTA 0 through distributed shared memory.  HBM-bound: 4 bytes
-// read per element, 8 bytes written per output entry.
+// in flight per thread, twice: the first pass forms (m, l) and each thread's
+// maximum, whose k-th largest within the warp is a threshold every top-k
+// entry reaches; the second pass (served mostly from L2, the slice was just
+// read) merges only entries that beat it into the warp's running list.  Lists
+// merge by k rounds of a warp-wide arg-max over the lanes' list heads; the
+// CTA's lists meet in shared memory and the cluster's in CTA 0 through
+// distributed shared memory.  HBM-bound: 4 bytes read per element once from
+// HBM, 8 bytes written per output entry.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -89,38 +93,38 @@ struct List {
   }
 };
 
-// The K best entries over the lists of all lanes of the warp, by K rounds of a
-// warp-wide arg-max over the list heads.  Rank r ends in lane r % 32 (slot 0
-// for r < 32, slot 1 for 32 <= r < 64).
-template <int K>
-__device__ __forceinline__ void warp_merge(List<K>& L, float& v0, int& i0, float& v1, int& i1) {
-  const int lane = threadIdx.x & 31;
-  v0 = v1 = kNegInf;
-  i0 = i1 = kNoIndex;
-#pragma unroll 1
-  for (int r = 0; r < K; ++r) {
-    float bv = L.v[0];
-    int bi = L.i[0];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      if (before(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if (bi != kNoIndex && L.i[0] == bi) L.pop();  // indices are unique within a row
-    if ((r & 31) == lane) {
-      if (r < 32) {
-        v0 = bv;
-        i0 = bi;
-      } else {
-        v1 = bv;
-        i1 = bi;
-      }
-    }
+// Lane-sorted lists of (value, index) pairs: lane r holds the r-th entry in
+// the total order above.  Compare-exchange with the partner lane^stride, keeping
+// the better entry when keep_best.
+__device__ __forceinline__ void cmpx_pair(float& v, int& i, int stride, bool keep_best) {
+  const float ov = __shfl_xor_sync(0xffffffffu, v, stride);
+  const int oi = __shfl_xor_sync(0xffffffffu, i, stride);
+  if (before(ov, oi, v, i) == keep_best) {
+    v = ov;
+    i = oi;
   }
+}
+// One pair per lane -> the warp's 32 pairs sorted (bitonic network, 15 stages).
+__device__ __forceinline__ void warp_sort_pairs(float& v, int& i) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size / 2; stride > 0; stride >>= 1)
+      cmpx_pair(v, i, stride, ((lane & stride) == 0) == ((lane & size) == 0));
+  }
+}
+// a <- the 32 best of the lane-sorted lists a and b, lane-sorted.
+__device__ __forceinline__ void warp_merge_pairs(float& av, int& ai, float bv, int bi) {
+  const int lane = threadIdx.x & 31;
+  const float rv = __shfl_sync(0xffffffffu, bv, 31 - lane);
+  const int ri = __shfl_sync(0xffffffffu, bi, 31 - lane);
+  if (!before(av, ai, rv, ri)) {  // the better of a[r] and b[31-r]: a bitonic sequence
+    av = rv;
+    ai = ri;
+  }
+#pragma unroll
+  for (int stride = 16; stride > 0; stride >>= 1) cmpx_pair(av, ai, stride, (lane & stride) == 0);
 }
 
 __device__ __forceinline__ float rebase(float m, float mn) {  // weight of a summary at max mn
@@ -154,44 +158,119 @@ __device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
   return v;
 }
 
-template <int K>
-struct Block {  // per (value, index) pair feeding: online (m, l) and the list
-  float m = kNegInf, l = 0.f;
-  List<K> L;
-  __device__ __forceinline__ void add4(float4 x, int j) {
-    const float mb = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
-    if (mb > m) {
-      l = (m == kNegInf) ? 0.f : l * ptx::ex2((m - mb) * kLog2e);
-      m = mb;
+// One value per lane -> the warp's 32 values sorted in descending order
+// (lane r holds the r-th largest): a bitonic network of 15 shuffle stages.
+__device__ __forceinline__ float warp_sort_desc(float v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size / 2; stride > 0; stride >>= 1) {
+      const float o = __shfl_xor_sync(0xffffffffu, v, stride);
+      const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
+      v = keep_max ? fmaxf(v, o) : fminf(v, o);
     }
-    if (m != kNegInf)
-      l += (ptx::ex2((x.x - m) * kLog2e) + ptx::ex2((x.y - m) * kLog2e)) +
-           (ptx::ex2((x.z - m) * kLog2e) + ptx::ex2((x.w - m) * kLog2e));
-    L.insert(x.x, j);
-    L.insert(x.y, j + 1);
-    L.insert(x.z, j + 2);
-    L.insert(x.w, j + 3);
   }
-  __device__ __forceinline__ void add1(float x, int j) {
-    if (x > m) {
-      l = (m == kNegInf) ? 0.f : l * ptx::ex2((m - x) * kLog2e);
-      m = x;
-    }
-    if (m != kNegInf) l += ptx::ex2((x - m) * kLog2e);
-    L.insert(x, j);
+  return v;
+}
+// The 32 largest of two descending lane-sorted lists, again lane-sorted.
+__device__ __forceinline__ float warp_merge_desc(float a, float b) {
+  const int lane = threadIdx.x & 31;
+  float c = fmaxf(a, __shfl_sync(0xffffffffu, b, 31 - lane));  // bitonic, holds the top 32
+#pragma unroll
+  for (int stride = 16; stride > 0; stride >>= 1) {
+    const float o = __shfl_xor_sync(0xffffffffu, c, stride);
+    c = (lane & stride) == 0 ? fmaxf(c, o) : fminf(c, o);
   }
-};
+  return c;
+}
 
+// The 32 best entries over the per-thread lists of a whole cluster, lane-sorted
+// in warp 0 of CTA 0.  Warp: the lanes' r-th entries are sorted as a batch and
+// merged into the running list, one batch per list depth in use; CTA: warp 0
+// merges the warps' lists from shared memory; cluster: CTA 0's warp 0 merges
+// the CTAs' lists through distributed shared memory.  One cluster barrier
+// inside; the caller adds another before the shared lists are written again.
+template <int K>
+__device__ __forceinline__ void cluster_topk(List<K>& L, float* s_pv, int* s_pi,
+                                             float* c_v, int* c_i, int nct, uint32_t rank,
+                                             float& av, int& ai) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  av = kNegInf;
+  ai = kNoIndex;
+#pragma unroll 1
+  for (int r = 0; r < K; ++r) {
+    if (!__any_sync(0xffffffffu, L.i[0] != kNoIndex)) break;  // lists are filled in order
+    float bv = L.v[0];
+    int bi = L.i[0];
+    L.pop();
+    warp_sort_pairs(bv, bi);
+    if (r == 0) {
+      av = bv;
+      ai = bi;
+    } else {
+      warp_merge_pairs(av, ai, bv, bi);
+    }
+  }
+  s_pv[warp * 32 + lane] = av;
+  s_pi[warp * 32 + lane] = ai;
+  __syncthreads();
+  if (warp == 0) {
+    av = s_pv[lane];
+    ai = s_pi[lane];
+    for (int w = 1; w < kWarps; ++w) warp_merge_pairs(av, ai, s_pv[w * 32 + lane], s_pi[w * 32 + lane]);
+    c_v[lane] = av;
+    c_i[lane] = ai;
+  }
+  cluster_sync_all();  // every CTA's list is visible to CTA 0
+  if (rank == 0 && warp == 0) {
+    for (int q = 1; q < nct; ++q)
+      warp_merge_pairs(av, ai, ld_cluster_f32(cluster_addr(&c_v[lane], q)),
+                       ld_cluster_s32(cluster_addr(&c_i[lane], q)));
+  }
+}
+
+// The 32 best entries of the cluster from each warp's lane-sorted list (av, ai),
+// lane-sorted in warp 0 of CTA 0; as the tail of cluster_topk.
+__device__ __forceinline__ void cluster_merge_lists(float& av, int& ai, float* s_pv, int* s_pi,
+                                                    float* c_v, int* c_i, int nct,
+                                                    uint32_t rank) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  s_pv[warp * 32 + lane] = av;
+  s_pi[warp * 32 + lane] = ai;
+  __syncthreads();
+  if (warp == 0) {
+    av = s_pv[lane];
+    ai = s_pi[lane];
+    for (int w = 1; w < kWarps; ++w) warp_merge_pairs(av, ai, s_pv[w * 32 + lane], s_pi[w * 32 + lane]);
+    c_v[lane] = av;
+    c_i[lane] = ai;
+  }
+  cluster_sync_all();  // every CTA's list is visible to CTA 0
+  if (rank == 0 && warp == 0) {
+    for (int q = 1; q < nct; ++q)
+      warp_merge_pairs(av, ai, ld_cluster_f32(cluster_addr(&c_v[lane], q)),
+                       ld_cluster_s32(cluster_addr(&c_i[lane], q)));
+  }
+}
+
+// Two passes over the CTA's slice of the row (the second mostly from L2):
+//  1. the online (m, l) and each thread's maximum; the K-th largest thread
+//     maximum of a warp is a threshold T with at least K entries of the warp
+//     >= T, so every entry of the row's top K is >= its warp's T;
+//  2. only entries that beat the warp's filter (T, then the K-th entry of the
+//     warp's running list) enter that list; the warps' lists merge into the
+//     row's top K.  K = 1 needs one pass: each thread's argmax.
 template <int K>
 __global__ void __launch_bounds__(kThreads) softmax_topk_kernel(const float* __restrict__ x,
                                                                 int64_t cols, int nct, int vec,
                                                                 int k, int32_t* __restrict__ idx,
                                                                 float* __restrict__ prob) {
-  __shared__ float s_v[kWarps][K];
-  __shared__ int s_i[kWarps][K];
+  __shared__ float s_pv[kWarps * 32];  // the warps' sorted lists
+  __shared__ int s_pi[kWarps * 32];
   __shared__ float s_m[kWarps], s_l[kWarps];
-  __shared__ float c_v[K];  // this CTA's list and summary, read by CTA 0 of the cluster
-  __shared__ int c_i[K];
+  __shared__ float c_v[32];  // this CTA's list and summary, read by CTA 0 of the cluster
+  __shared__ int c_i[32];
   __shared__ float c_ml[2];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -202,28 +281,78 @@ __global__ void __launch_bounds__(kThreads) softmax_topk_kernel(const float* __r
   const int64_t chunk = ((cols + nct - 1) / nct + 3) / 4 * 4;
   const int64_t c0 = rank * chunk < cols ? rank * chunk : cols;
   const int64_t c1 = c0 + chunk < cols ? c0 + chunk : cols;
+  const float4* x4 = reinterpret_cast<const float4*>(xr);
+  const int64_t f0 = c0 / 4, f1 = c1 / 4;
 
-  Block<K> st;
-  st.L.clear();
+  // ---- pass 1: (m, l) and the thread maximum
+  float m = kNegInf, l = 0.f;
+  float bv = kNegInf;  // K == 1: the thread's best entry (elements arrive in column order)
+  int bi = kNoIndex;
+  auto best = [&](float v, int j) {
+    if constexpr (K == 1) {
+      if (v > bv || bi == kNoIndex) {
+        bv = v;
+        bi = j;
+      }
+    }
+  };
+  auto add1 = [&](float v) {
+    if (v > m) {
+      l = (m == kNegInf) ? 0.f : l * ptx::ex2((m - v) * kLog2e);
+      m = v;
+    }
+    if (m != kNegInf) l += ptx::ex2((v - m) * kLog2e);
+  };
+  auto add4 = [&](float4 v) {
+    const float mb = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+    if (mb > m) {
+      l = (m == kNegInf) ? 0.f : l * ptx::ex2((m - mb) * kLog2e);
+      m = mb;
+    }
+    if (m != kNegInf)
+      l += (ptx::ex2((v.x - m) * kLog2e) + ptx::ex2((v.y - m) * kLog2e)) +
+           (ptx::ex2((v.z - m) * kLog2e) + ptx::ex2((v.w - m) * kLog2e));
+  };
   if (vec) {
-    const float4* x4 = reinterpret_cast<const float4*>(xr);
-    const int64_t f0 = c0 / 4, f1 = c1 / 4;
     int64_t f = f0 + tid;
     for (; f + 3 * kThreads < f1; f += 4 * kThreads) {  // four 16-byte loads in flight
-      const float4 a = __ldcs(x4 + f), b = __ldcs(x4 + f + kThreads);
-      const float4 c = __ldcs(x4 + f + 2 * kThreads), d = __ldcs(x4 + f + 3 * kThreads);
-      st.add4(a, static_cast<int>(4 * f));
-      st.add4(b, static_cast<int>(4 * (f + kThreads)));
-      st.add4(c, static_cast<int>(4 * (f + 2 * kThreads)));
-      st.add4(d, static_cast<int>(4 * (f + 3 * kThreads)));
+      const float4 a = x4[f], b = x4[f + kThreads];
+      const float4 c = x4[f + 2 * kThreads], d = x4[f + 3 * kThreads];
+      add4(a);
+      add4(b);
+      add4(c);
+      add4(d);
+      if constexpr (K == 1) {
+        const float4 e[4] = {a, b, c, d};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j = static_cast<int>(4 * (f + u * kThreads));
+          best(e[u].x, j);
+          best(e[u].y, j + 1);
+          best(e[u].z, j + 2);
+          best(e[u].w, j + 3);
+        }
+      }
     }
-    for (; f < f1; f += kThreads) st.add4(__ldcs(x4 + f), static_cast<int>(4 * f));
+    for (; f < f1; f += kThreads) {
+      const float4 a = x4[f];
+      add4(a);
+      const int j = static_cast<int>(4 * f);
+      best(a.x, j);
+      best(a.y, j + 1);
+      best(a.z, j + 2);
+      best(a.w, j + 3);
+    }
   } else {
-    for (int64_t j = c0 + tid; j < c1; j += kThreads) st.add1(__ldcs(xr + j), static_cast<int>(j));
+    for (int64_t j = c0 + tid; j < c1; j += kThreads) {
+      const float a = xr[j];
+      add1(a);
+      best(a, static_cast<int>(j));
+    }
   }
+  const float tmax = m;  // the running max is the thread's maximum
 
-  // warp: (m, l) by shuffles, lists by K rounds
-  float m = st.m, l = st.l;
+  // warp (m, l)
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     const float mo = __shfl_xor_sync(0xffffffffu, m, off);
@@ -232,43 +361,19 @@ __global__ void __launch_bounds__(kThreads) softmax_topk_kernel(const float* __r
     l = l * rebase(m, mn) + lo * rebase(mo, mn);
     m = mn;
   }
-  float v0, v1;
-  int i0, i1;
-  warp_merge<K>(st.L, v0, i0, v1, i1);
-  if (lane < K) {
-    s_v[warp][lane] = v0;
-    s_i[warp][lane] = i0;
-  }
-  if (lane + 32 < K) {
-    s_v[warp][lane + 32] = v1;
-    s_i[warp][lane + 32] = i1;
-  }
   if (lane == 0) {
     s_m[warp] = m;
     s_l[warp] = l;
   }
-  __syncthreads();
-  // CTA: warp 0 merges the warps' lists (lane w holds warp w's list)
-  if (warp == 0) {
-    List<K> L;
-    L.clear();
-    if (lane < kWarps) {
-#pragma unroll
-      for (int s = 0; s < K; ++s) {
-        L.v[s] = s_v[lane][s];
-        L.i[s] = s_i[lane][s];
-      }
-    }
-    warp_merge<K>(L, v0, i0, v1, i1);
-    if (lane < K) {
-      c_v[lane] = v0;
-      c_i[lane] = i0;
-    }
-    if (lane + 32 < K) {
-      c_v[lane + 32] = v1;
-      c_i[lane + 32] = i1;
-    }
-    if (lane == 0) {
+
+  List<K> L;
+  L.clear();
+  float v0;
+  int i0;
+  if constexpr (K == 1) {
+    // the best entry is the thread's argmax; no threshold, no second pass
+    __syncthreads();
+    if (tid == 0) {  // the CTA's (m, l), read by CTA 0 at the end
       float M = s_m[0], Ls = s_l[0];
       for (int w = 1; w < kWarps; ++w) {
         const float mn = fmaxf(M, s_m[w]);
@@ -278,19 +383,118 @@ __global__ void __launch_bounds__(kThreads) softmax_topk_kernel(const float* __r
       c_ml[0] = M;
       c_ml[1] = Ls;
     }
+    L.v[0] = bv;
+    L.i[0] = bi;
+  } else {
+  // ---- threshold: the K-th largest thread maximum of the warp.  At least K
+  // entries of the warp reach it, so an entry below it has K better ones in
+  // its own warp and cannot be among the row's K best.
+  const float wsorted = warp_sort_desc(tmax);
+  float thr = __shfl_sync(0xffffffffu, wsorted, K - 1);  // K <= 32
+  if constexpr (K > 16) {
+    // a warp's K-th lane maximum is weak for large K: also take the CTA's
+    // K-th thread maximum (merged by warp 0); either bound is valid
+    s_pv[warp * 32 + lane] = wsorted;
+    __syncthreads();
+    if (warp == 0) {
+      float acc = s_pv[lane];
+      for (int w = 1; w < kWarps; ++w) acc = warp_merge_desc(acc, s_pv[w * 32 + lane]);
+      const float t = __shfl_sync(0xffffffffu, acc, K - 1);
+      if (lane == 0) c_ml[0] = t;  // staged here until the summary is written
+    }
+    __syncthreads();
+    thr = fmaxf(thr, c_ml[0]);
   }
-  cluster_sync_all();  // every CTA's list and summary are visible to CTA 0
-  if (rank == 0 && warp == 0) {
-    List<K> L;
-    L.clear();
-    if (lane < nct) {
+  __syncthreads();
+  if (tid == 0) {  // the CTA's (m, l), read by CTA 0 at the end
+    float M = s_m[0], Ls = s_l[0];
+    for (int w = 1; w < kWarps; ++w) {
+      const float mn = fmaxf(M, s_m[w]);
+      Ls = Ls * rebase(M, mn) + s_l[w] * rebase(s_m[w], mn);
+      M = mn;
+    }
+    c_ml[0] = M;
+    c_ml[1] = Ls;
+  }
+
+  // ---- pass 2: entries that beat the filter enter the warp's running best 32
+  // (lane-sorted).  The filter starts at (thr, any index) and tightens to the
+  // list's K-th entry in the (value, index) order, so later ties and weaker
+  // values drop out.  Each round every lane offers one candidate; the batch is
+  // sorted and merged into the list.
+  {
+    float kv = thr;
+    int ki = kNoIndex;
+    auto round = [&](float cv, int ci) {
+      warp_sort_pairs(cv, ci);
+      warp_merge_pairs(v0, i0, cv, ci);
+      const float nv = __shfl_sync(0xffffffffu, v0, K - 1);
+      const int ni = __shfl_sync(0xffffffffu, i0, K - 1);
+      if (ni != kNoIndex && before(nv, ni, kv, ki)) {
+        kv = nv;
+        ki = ni;
+      }
+    };
+    v0 = kNegInf;
+    i0 = kNoIndex;
+    if (vec) {
+      for (int64_t f = f0 + tid; f - tid < f1; f += 4 * kThreads) {
+        float4 a[4];
 #pragma unroll
-      for (int s = 0; s < K; ++s) {
-        L.v[s] = ld_cluster_f32(cluster_addr(&c_v[s], lane));
-        L.i[s] = ld_cluster_s32(cluster_addr(&c_i[s], lane));
+        for (int u = 0; u < 4; ++u)
+          a[u] = f + u * kThreads < f1 ? __ldcs(x4 + f + u * kThreads)
+                                       : make_float4(kNegInf, kNegInf, kNegInf, kNegInf);
+        uint32_t msk = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (f + u * kThreads >= f1) continue;  // past the slice: no entry
+          msk |= (a[u].x >= kv ? 1u : 0u) << (4 * u);
+          msk |= (a[u].y >= kv ? 2u : 0u) << (4 * u);
+          msk |= (a[u].z >= kv ? 4u : 0u) << (4 * u);
+          msk |= (a[u].w >= kv ? 8u : 0u) << (4 * u);
+        }
+        while (__any_sync(0xffffffffu, msk != 0)) {
+          float cv = kNegInf;
+          int ci = kNoIndex;
+          while (msk) {  // this lane's next entry that still beats the filter
+            const int e = __ffs(msk) - 1;
+            msk &= msk - 1;
+            const int u = e >> 2, c = e & 3;
+            float4 w = a[0];
+            if (u == 1) w = a[1];
+            if (u == 2) w = a[2];
+            if (u == 3) w = a[3];
+            float v = w.x;
+            if (c == 1) v = w.y;
+            if (c == 2) v = w.z;
+            if (c == 3) v = w.w;
+            const int j = static_cast<int>(4 * (f + u * kThreads)) + c;
+            if (before(v, j, kv, ki)) {
+              cv = v;
+              ci = j;
+              break;
+            }
+          }
+          round(cv, ci);
+        }
+      }
+    } else {
+      for (int64_t j0 = c0; j0 < c1; j0 += kThreads) {
+        const int64_t j = j0 + tid;
+        const float a = j < c1 ? __ldcs(xr + j) : kNegInf;
+        const bool cand = j < c1 && before(a, static_cast<int>(j), kv, ki);
+        if (__any_sync(0xffffffffu, cand))
+          round(cand ? a : kNegInf, cand ? static_cast<int>(j) : kNoIndex);
       }
     }
-    warp_merge<K>(L, v0, i0, v1, i1);
+  }
+  }  // K > 1
+  if constexpr (K == 1) {
+    cluster_topk<K>(L, s_pv, s_pi, c_v, c_i, nct, rank, v0, i0);
+  } else {
+    cluster_merge_lists(v0, i0, s_pv, s_pi, c_v, c_i, nct, rank);
+  }
+  if (rank == 0 && warp == 0) {
     // the row's (M, L), merged in rank order
     float M = kNegInf, Ls = 0.f;
     for (int q = 0; q < nct; ++q) {
@@ -306,10 +510,6 @@ __global__ void __launch_bounds__(kThreads) softmax_topk_kernel(const float* __r
     if (lane < k) {
       irow[lane] = i0;
       prow[lane] = (Ls > 0.f && v0 != kNegInf) ? exp_le0(v0 - M) * inv : 0.f;
-    }
-    if (lane + 32 < k) {
-      irow[lane + 32] = i1;
-      prow[lane + 32] = (Ls > 0.f && v1 != kNegInf) ? exp_le0(v1 - M) * inv : 0.f;
     }
   }
   cluster_sync_all();  // CTA 0 has read every CTA's shared memory
