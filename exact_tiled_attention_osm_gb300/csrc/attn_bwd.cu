@@ -44,7 +44,12 @@ constexpr int kTile = 128;   // rows of every tile (query or key)
 constexpr int kSlots = 4;    // streamed 32 KB tiles in flight
 constexpr uint32_t kTileBytes = kTile * kHeadDim * 2;  // 32768
 constexpr uint32_t kBoxBytes = 128 * 64 * 2;           // one TMA box: 64 columns x 128 rows
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 4-11 element-wise
+// The element-wise warps: two per TMEM lane quarter, warp 4 + q + 4h takes
+// columns 64h .. 64h+63 of rows 32q .. 32q+31.  Each writes its packed bf16
+// results inside its own half (chunk c of 32 columns at 64(c/2) + 16(c%2)),
+// so neither overwrites columns the other has not read yet; the products that
+// read them address 16-column step kk at tmem_half_col(kk).
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kPosInf = __builtin_huge_valf();
@@ -67,8 +72,8 @@ constexpr uint32_t kSmemTmemSlot = kSmemBar + 8 * NUM_BARS;
 constexpr uint32_t kSmemAbort = kSmemTmemSlot + 4;
 // per softmax warp: [2 buffers][lse2 | D][128 columns] floats
 constexpr uint32_t kSmemCol = (kSmemAbort + 4 + 15) / 16 * 16;
-constexpr uint32_t kColFloats = 2 * 2 * kTile;
-constexpr uint32_t kSmemBytes = kSmemCol + 4 * kColFloats * 4 + 1024;
+constexpr uint32_t kColFloats = 2 * 2 * (kTile / 2);
+constexpr uint32_t kSmemBytes = kSmemCol + 8 * kColFloats * 4 + 1024;
 
 constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemAcc0 = 256, kTmemAcc1 = 384;
 
@@ -97,11 +102,15 @@ __device__ __forceinline__ int key_len_of(const Params& p, int b) {
   return L < 0 ? 0 : (L > p.Nk ? p.Nk : L);
 }
 
-// 16-byte global stores of one 128-column bf16 row from four 32-column TMEM chunks
+__host__ __device__ constexpr uint32_t tmem_half_col(int kk) {
+  return static_cast<uint32_t>(64 * (kk >> 2) + 8 * (kk & 3));
+}
+
+// 16-byte global stores of 32-column chunks c0 .. c1-1 of one bf16 row from TMEM
 __device__ __forceinline__ void store_row_bf16(uint32_t t_acc, float mul, __nv_bfloat16* dst,
-                                               bool ok) {
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
+                                               bool ok, int c0 = 0, int c1 = 4) {
+#pragma unroll 1
+  for (int c = c0; c < c1; ++c) {
     uint32_t r[32];
     tmem_ld_x32(t_acc + 32 * c, r);
     if (ok) {
@@ -178,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_kv = (kend + kTile - 1) / kTile;
 
   if (n_kv == 0) {  // no visible key for any row of the tile: dQ = 0
-    if (warp >= 4) {
+    if (warp >= 4 && warp < 8) {
       const int row = q0 + 32 * (warp - 4) + lane;
       if (row < p.Nq) zero_row_bf16(p.dq + (static_cast<int64_t>(bh) * p.Nq + row) * kHeadDim);
     }
@@ -193,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(RING_EMPTY + s), 1);
     }
     mbar_init(bar(S_FULL), 1);
-    mbar_init(bar(P_FULL), 4);
+    mbar_init(bar(P_FULL), 8);
     mbar_init(bar(O_FULL), 1);
     mbar_init(bar(DRAIN), 1);
     fence_mbar_init();
@@ -259,8 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t kdesc = dMN + ((sRing + k_prev * kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tbase + kTmemAcc0, tbase + kTmemS + kk * 8, kdesc + ((kk * 2048) >> 4), kIdescKMN,
-                 (jj > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tbase + kTmemAcc0, tbase + kTmemS + tmem_half_col(kk), kdesc + ((kk * 2048) >> 4),
+                 kIdescKMN, (jj > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(RING_EMPTY + k_prev));  // K_{j-1} is free after this product
         return true;
       };
@@ -297,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------- P and dS
-    const int wq = warp & 3;
+    const int wq = warp & 3, hh = (warp - 4) >> 2;  // lane quarter, column half
     const uint32_t lane_off = static_cast<uint32_t>(32 * wq) << 16;
     const uint32_t tS = tbase + lane_off + kTmemS, tDP = tbase + lane_off + kTmemDP;
     const int row = q0 + 32 * wq + lane;
@@ -319,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int k0 = j * kTile;
       const bool masked_tile = __any_sync(0xffffffffu, k0 + kTile > limit);
 #pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 2 * hh; ch < 2 * hh + 2; ++ch) {
         uint32_t s[32], dp[32], pk[16];
         tmem_ld_x32(tS + 32 * ch, s);
         tmem_ld_x32(tDP + 32 * ch, dp);
@@ -336,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __nv_bfloat162 h2 = __floats2bfloat162_rn(g0, g1);
           pk[e >> 1] = *reinterpret_cast<uint32_t*>(&h2);
         }
-        tmem_st_x16_nowait(tS + 16 * ch, pk);  // dS over S columns already read
+        tmem_st_x16_nowait(tS + 64 * hh + 16 * (ch & 1), pk);  // dS over this half's S, already read
       }
       tmem_wait_st();
       tc_fence_before();
@@ -347,7 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       tc_fence_after();
       store_row_bf16(tbase + lane_off + kTmemAcc0, p.scale,
-                     p.dq + (static_cast<int64_t>(bh) * p.Nq + row) * kHeadDim, row_ok);
+                     p.dq + (static_cast<int64_t>(bh) * p.Nq + row) * kHeadDim, row_ok, 2 * hh,
+                     2 * hh + 2);
     }
   }
   tc_fence_before();
@@ -385,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_q = (k0 < L && (!p.causal || k0 - off < p.Nq)) ? p.n_qt - qt_first : 0;
 
   if (n_q == 0) {  // every key of the tile is invisible to every query: dK = dV = 0
-    if (warp >= 4) {
+    if (warp >= 4 && warp < 8) {
       const int key = k0 + 32 * (warp - 4) + lane;
       if (key < p.Nk) {
         const int64_t g = (static_cast<int64_t>(bh) * p.Nk + key) * kHeadDim;
@@ -404,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(RING_EMPTY + s), 1);
     }
     mbar_init(bar(S_FULL), 1);
-    mbar_init(bar(P_FULL), 4);
+    mbar_init(bar(P_FULL), 8);
     mbar_init(bar(O_FULL), 1);
     mbar_init(bar(DRAIN), 1);
     fence_mbar_init();
@@ -472,12 +482,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t qd = dMN + ((sRing + q_prev * kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tbase + kTmemAcc0, tbase + kTmemS + kk * 8, dod + ((kk * 2048) >> 4), kIdescKMN,
-                 (ii > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tbase + kTmemAcc0, tbase + kTmemS + tmem_half_col(kk), dod + ((kk * 2048) >> 4),
+                 kIdescKMN, (ii > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tbase + kTmemAcc1, tbase + kTmemDP + kk * 8, qd + ((kk * 2048) >> 4), kIdescKMN,
-                 (ii > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tbase + kTmemAcc1, tbase + kTmemDP + tmem_half_col(kk), qd + ((kk * 2048) >> 4),
+                 kIdescKMN, (ii > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(RING_EMPTY + q_prev));
         mma_commit(bar(RING_EMPTY + do_prev));
         return true;
@@ -515,22 +525,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------- P^T and dS^T
-    const int wq = warp & 3;
-    const int tid = threadIdx.x - 128;  // 0..127: this thread's key row
+    const int wq = warp & 3, hh = (warp - 4) >> 2;  // lane quarter, column half
+    const int tid = 32 * wq + lane;  // 0..127: this thread's key row
     const uint32_t lane_off = static_cast<uint32_t>(32 * wq) << 16;
     const uint32_t tS = tbase + lane_off + kTmemS, tDP = tbase + lane_off + kTmemDP;
     const int key = k0 + tid;
     const bool key_ok = key < L;  // keys past the valid length see no query
     const float sl2 = p.scale_log2;
     const int64_t hrow = static_cast<int64_t>(bh) * p.Nq;
-    // Per-column lse (base 2) and D of query tile i.  Every warp stages its
-    // own copy in shared memory (lane l loads columns 4l..4l+3), so only
-    // __syncwarp is needed; the next tile's values load while this one runs.
-    float* colw = col + wq * kColFloats;
-    auto col_vals = [&](int i, float (&l2)[4], float (&dd)[4]) {
+    // Per-column lse (base 2) and D of this warp's 64 columns of query tile i.
+    // Every warp stages its own copy in shared memory (lane l loads columns
+    // 2l, 2l+1 of its half), so only __syncwarp is needed; the next tile's
+    // values load while this one runs.
+    float* colw = col + (warp - 4) * kColFloats;
+    auto col_vals = [&](int i, float (&l2)[2], float (&dd)[2]) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int q = (qt_first + i) * kTile + 4 * lane + u;
+      for (int u = 0; u < 2; ++u) {
+        const int q = (qt_first + i) * kTile + 64 * hh + 2 * lane + u;
         if (q < p.Nq) {
           l2[u] = p.lse[hrow + q] * kLog2e;
           if (!(l2[u] > kNegInf)) l2[u] = kPosInf;  // a query with no visible key: P = 0
@@ -541,16 +552,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     };
-    float nl2[4], nd[4];
+    float nl2[2], nd[2];
     col_vals(0, nl2, nd);
     uint32_t sf_ph = 0;
     bool ok = true;
     for (int i = 0; i < n_q; ++i) {
-      float* cl = colw + (i & 1) * 2 * kTile;
+      float* cl = colw + (i & 1) * kTile;  // [lse2 | D] x 64 columns
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        cl[4 * lane + u] = nl2[u];
-        cl[kTile + 4 * lane + u] = nd[u];
+      for (int u = 0; u < 2; ++u) {
+        cl[2 * lane + u] = nl2[u];
+        cl[kTile / 2 + 2 * lane + u] = nd[u];
       }
       __syncwarp();
       if (i + 1 < n_q) col_vals(i + 1, nl2, nd);
@@ -562,12 +573,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the tile needs the causal mask when some (key, query) pair is hidden
       const bool masked_tile = p.causal && __any_sync(0xffffffffu, key > qb + off);
 #pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 2 * hh; ch < 2 * hh + 2; ++ch) {
         uint32_t s[32], dp[32], pk[16], gk[16];
         tmem_ld_x32(tS + 32 * ch, s);
         tmem_ld_x32(tDP + 32 * ch, dp);
-        const float4* cl4 = reinterpret_cast<const float4*>(cl + 32 * ch);
-        const float4* cd4 = reinterpret_cast<const float4*>(cl + kTile + 32 * ch);
+        const float4* cl4 = reinterpret_cast<const float4*>(cl + 32 * (ch & 1));
+        const float4* cd4 = reinterpret_cast<const float4*>(cl + kTile / 2 + 32 * (ch & 1));
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
           const float4 l4 = cl4[e4], d4 = cd4[e4];
@@ -591,8 +602,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           gk[2 * e4] = *reinterpret_cast<uint32_t*>(&g0);
           gk[2 * e4 + 1] = *reinterpret_cast<uint32_t*>(&g1);
         }
-        tmem_st_x16_nowait(tS + 16 * ch, pk);   // P^T over S^T columns already read
-        tmem_st_x16_nowait(tDP + 16 * ch, gk);  // dS^T over dP^T columns already read
+        // P^T and dS^T over this half's S^T and dP^T columns, already read
+        tmem_st_x16_nowait(tS + 64 * hh + 16 * (ch & 1), pk);
+        tmem_st_x16_nowait(tDP + 64 * hh + 16 * (ch & 1), gk);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -604,8 +616,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const bool st_ok = key < p.Nk;
       const int64_t g = (static_cast<int64_t>(bh) * p.Nk + (st_ok ? key : 0)) * kHeadDim;
-      store_row_bf16(tbase + lane_off + kTmemAcc0, 1.f, p.dv + g, st_ok);
-      store_row_bf16(tbase + lane_off + kTmemAcc1, p.scale, p.dk + g, st_ok);
+      if (hh == 0)
+        store_row_bf16(tbase + lane_off + kTmemAcc0, 1.f, p.dv + g, st_ok);
+      else
+        store_row_bf16(tbase + lane_off + kTmemAcc1, p.scale, p.dk + g, st_ok);
     }
   }
   tc_fence_before();
