@@ -315,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float lse2 = row_ok ? p.lse[grow] * kLog2e : kPosInf;
     if (!(lse2 > kNegInf)) lse2 = kPosInf;  // a row with no visible key: every P is 0
     const float dlt = row_ok ? p.delta[grow] : 0.f;
+    const float nlse2 = -lse2, ndlt = -dlt;
     int limit = L;
     if (p.causal) limit = min(limit, row + 1 + (p.Nk - p.Nq));
     const float sl2 = p.scale_log2;
@@ -330,18 +331,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int ch = 2 * hh; ch < 2 * hh + 2; ++ch) {
         uint32_t s[32], dp[32], pk[16];
-        tmem_ld_x32(tS + 32 * ch, s);
-        tmem_ld_x32(tDP + 32 * ch, dp);
+        tmem_ld_x32_nowait(tS + 32 * ch, s);  // both loads in flight, one wait
+        tmem_ld_x32_nowait(tDP + 32 * ch, dp);
+        tmem_wait_ld_dep32(s);
+        tmem_wait_ld_dep32(dp);
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float p0 = ex2(fmaf(__uint_as_float(s[e]), sl2, -lse2));
-          float p1 = ex2(fmaf(__uint_as_float(s[e + 1]), sl2, -lse2));
+          float x0, x1, t0 = __uint_as_float(dp[e]), t1 = __uint_as_float(dp[e + 1]), g0, g1;
+          fma2(x0, x1, __uint_as_float(s[e]), __uint_as_float(s[e + 1]), sl2, sl2, nlse2, nlse2);
+          float p0 = ex2(x0), p1 = ex2(x1);
           if (masked_tile) {
             if (k0 + 32 * ch + e >= limit) p0 = 0.f;
             if (k0 + 32 * ch + e + 1 >= limit) p1 = 0.f;
           }
-          const float g0 = p0 * (__uint_as_float(dp[e]) - dlt);
-          const float g1 = p1 * (__uint_as_float(dp[e + 1]) - dlt);
+          add2(t0, t1, ndlt, ndlt);  // dP - D
+          fma2(g0, g1, t0, t1, p0, p1, 0.f, 0.f);
           __nv_bfloat162 h2 = __floats2bfloat162_rn(g0, g1);
           pk[e >> 1] = *reinterpret_cast<uint32_t*>(&h2);
         }
@@ -542,12 +546,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int q = (qt_first + i) * kTile + 64 * hh + 2 * lane + u;
+        // stored negated: -lse2 and -D enter packed adds directly
         if (q < p.Nq) {
-          l2[u] = p.lse[hrow + q] * kLog2e;
-          if (!(l2[u] > kNegInf)) l2[u] = kPosInf;  // a query with no visible key: P = 0
-          dd[u] = p.delta[hrow + q];
+          l2[u] = -p.lse[hrow + q] * kLog2e;
+          if (!(l2[u] < kPosInf)) l2[u] = kNegInf;  // a query with no visible key: P = 0
+          dd[u] = -p.delta[hrow + q];
         } else {
-          l2[u] = kPosInf;
+          l2[u] = kNegInf;
           dd[u] = 0.f;
         }
       }
@@ -572,27 +577,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qb = (qt_first + i) * kTile;
       // the tile needs the causal mask when some (key, query) pair is hidden
       const bool masked_tile = p.causal && __any_sync(0xffffffffu, key > qb + off);
+      const bool need_mask = masked_tile || __any_sync(0xffffffffu, !key_ok);
 #pragma unroll 1
       for (int ch = 2 * hh; ch < 2 * hh + 2; ++ch) {
         uint32_t s[32], dp[32], pk[16], gk[16];
-        tmem_ld_x32(tS + 32 * ch, s);
-        tmem_ld_x32(tDP + 32 * ch, dp);
+        tmem_ld_x32_nowait(tS + 32 * ch, s);  // both loads in flight, one wait
+        tmem_ld_x32_nowait(tDP + 32 * ch, dp);
+        tmem_wait_ld_dep32(s);
+        tmem_wait_ld_dep32(dp);
         const float4* cl4 = reinterpret_cast<const float4*>(cl + 32 * (ch & 1));
         const float4* cd4 = reinterpret_cast<const float4*>(cl + kTile / 2 + 32 * (ch & 1));
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 l4 = cl4[e4], d4 = cd4[e4];
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pr[4], gr[4];
+          const float4 l4 = cl4[e4], d4 = cd4[e4];  // -lse2, -D of four columns
+          const int e = 4 * e4;
+          float x[4], pr[4], t[4], gr[4];
+          fma2(x[0], x[1], __uint_as_float(s[e]), __uint_as_float(s[e + 1]), sl2, sl2, l4.x, l4.y);
+          fma2(x[2], x[3], __uint_as_float(s[e + 2]), __uint_as_float(s[e + 3]), sl2, sl2, l4.z, l4.w);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int e = 4 * e4 + u;
-            float pe = ex2(fmaf(__uint_as_float(s[e]), sl2, -lv[u]));
-            if (!key_ok) pe = 0.f;
-            if (masked_tile && key > qb + 32 * ch + e + off) pe = 0.f;
-            pr[u] = pe;
-            gr[u] = pe * (__uint_as_float(dp[e]) - dv[u]);
+          for (int u = 0; u < 4; ++u) pr[u] = ex2(x[u]);
+          if (need_mask) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              if (!key_ok || (masked_tile && key > qb + 32 * ch + e + u + off)) pr[u] = 0.f;
           }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) t[u] = __uint_as_float(dp[e + u]);
+          add2(t[0], t[1], d4.x, d4.y);  // dP - D
+          add2(t[2], t[3], d4.z, d4.w);
+          fma2(gr[0], gr[1], t[0], t[1], pr[0], pr[1], 0.f, 0.f);
+          fma2(gr[2], gr[3], t[2], t[3], pr[2], pr[3], 0.f, 0.f);
           __nv_bfloat162 a0 = __floats2bfloat162_rn(pr[0], pr[1]);
           __nv_bfloat162 a1 = __floats2bfloat162_rn(pr[2], pr[3]);
           __nv_bfloat162 g0 = __floats2bfloat162_rn(gr[0], gr[1]);
