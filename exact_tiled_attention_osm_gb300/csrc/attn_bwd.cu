@@ -66,6 +66,8 @@ enum Bar : uint32_t {
   P_FULL = S_FULL + 1,
   O_FULL = P_FULL + 1,
   DRAIN = O_FULL + 1,
+  DP_FULL = DRAIN + 1,   // dK/dV kernel: dP^T ready (S_FULL then only S^T)
+  DS_FULL = DP_FULL + 1, // dK/dV kernel: dS^T written
   NUM_BARS
 };
 constexpr uint32_t kSmemTmemSlot = kSmemBar + 8 * NUM_BARS;
@@ -418,7 +420,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(RING_EMPTY + s), 1);
     }
     mbar_init(bar(S_FULL), 1);
+    mbar_init(bar(DP_FULL), 1);
     mbar_init(bar(P_FULL), 8);
+    mbar_init(bar(DS_FULL), 8);
     mbar_init(bar(O_FULL), 1);
     mbar_init(bar(DRAIN), 1);
     fence_mbar_init();
@@ -469,59 +473,81 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------- MMA issuer
+    // Order per query tile i: S_i, dP_i | dV_i (after P_i) | S_{i+1} | dK_i
+    // (after dS_i) | dP_{i+1}.  Each element-wise phase overlaps two products,
+    // and every product that overwrites a TMEM region is issued after the
+    // product that reads it (the tensor pipe runs them in issue order).
     const uint64_t dKm = sdesc_sw128(0, 16, 1024);
     const uint64_t dMN = sdesc_sw128(0, 16384, 1024);
     bool ok = wait_one(bar(RES_FULL), 0, kSiteK | 2);
-    uint32_t slot = 0, ph = 0, pf_ph = 0;
-    uint32_t q_prev = 0, do_prev = 0;
+    uint32_t slot = 0, ph = 0, pf_ph = 0, df_ph = 0;
     if (ok) {
       tc_fence_after();
       const uint64_t kdesc = dKm + (sK >> 4), vdesc = dKm + (sV >> 4);
-      // dV += P^T_{i-1} dO_{i-1}, dK += dS^T_{i-1} Q_{i-1}
-      auto issue_acc = [&](int ii) -> bool {
-        if (!wait_one(bar(P_FULL), pf_ph, kSiteK | 3)) return false;
-        pf_ph ^= 1;
-        tc_fence_after();
-        const uint64_t dod = dMN + ((sRing + do_prev * kTileBytes) >> 4);
-        const uint64_t qd = dMN + ((sRing + q_prev * kTileBytes) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tbase + kTmemAcc0, tbase + kTmemS + tmem_half_col(kk), dod + ((kk * 2048) >> 4),
-                 kIdescKMN, (ii > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tbase + kTmemAcc1, tbase + kTmemDP + tmem_half_col(kk), qd + ((kk * 2048) >> 4),
-                 kIdescKMN, (ii > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(RING_EMPTY + q_prev));
-        mma_commit(bar(RING_EMPTY + do_prev));
-        return true;
+      auto next_slot = [&](uint32_t& s_out) -> bool {  // ring slots in fill order
+        s_out = slot;
+        const bool r = wait_one(bar(RING_FULL + slot), ph, kSiteK | 4);
+        if (++slot == kSlots) { slot = 0; ph ^= 1; }
+        return r;
       };
-      for (int i = 0; ok && i < n_q; ++i) {
-        const uint32_t qs = slot;
-        if (!(ok = wait_one(bar(RING_FULL + qs), ph, kSiteK | 4))) break;
-        if (++slot == kSlots) { slot = 0; ph ^= 1; }
-        const uint32_t ds = slot;
-        if (!(ok = wait_one(bar(RING_FULL + ds), ph, kSiteK | 4))) break;
-        if (++slot == kSlots) { slot = 0; ph ^= 1; }
-        if (i > 0 && !(ok = issue_acc(i - 1))) break;
+      auto issue_s = [&](uint32_t qs) {  // S^T = K Q_i^T
         tc_fence_after();
         const uint64_t qdesc = dKm + ((sRing + qs * kTileBytes) >> 4);
-        const uint64_t dodesc = dKm + ((sRing + ds * kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 16; ++kk) {
           const uint32_t o16 = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
           mma_ss(tbase + kTmemS, kdesc + o16, qdesc + o16, kIdescKK, kk > 0 ? 1u : 0u);
         }
+        mma_commit(bar(S_FULL));
+      };
+      auto issue_dp = [&](uint32_t ds) {  // dP^T = V dO_i^T
+        tc_fence_after();
+        const uint64_t dodesc = dKm + ((sRing + ds * kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 16; ++kk) {
           const uint32_t o16 = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
           mma_ss(tbase + kTmemDP, vdesc + o16, dodesc + o16, kIdescKK, kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar(S_FULL));
-        q_prev = qs;
-        do_prev = ds;
+        mma_commit(bar(DP_FULL));
+      };
+      uint32_t qs = 0, ds = 0;
+      if ((ok = next_slot(qs))) issue_s(qs);
+      if (ok && (ok = next_slot(ds))) issue_dp(ds);
+      for (int i = 0; ok && i < n_q; ++i) {
+        const bool more = i + 1 < n_q;
+        uint32_t qn = 0, dn = 0;
+        // dV += P_i^T dO_i once the element-wise warps have written P_i
+        if (!(ok = wait_one(bar(P_FULL), pf_ph, kSiteK | 3))) break;
+        pf_ph ^= 1;
+        tc_fence_after();
+        const uint64_t dod = dMN + ((sRing + ds * kTileBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tbase + kTmemAcc0, tbase + kTmemS + tmem_half_col(kk), dod + ((kk * 2048) >> 4),
+                 kIdescKMN, (i > 0 || kk > 0) ? 1u : 0u);
+        if (more) {
+          if (!(ok = next_slot(qn))) break;
+          issue_s(qn);
+        }
+        // dK += dS_i^T Q_i once they have written dS_i
+        if (!(ok = wait_one(bar(DS_FULL), df_ph, kSiteK | 7))) break;
+        df_ph ^= 1;
+        tc_fence_after();
+        const uint64_t qd = dMN + ((sRing + qs * kTileBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tbase + kTmemAcc1, tbase + kTmemDP + tmem_half_col(kk), qd + ((kk * 2048) >> 4),
+                 kIdescKMN, (i > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(RING_EMPTY + qs));
+        mma_commit(bar(RING_EMPTY + ds));
+        if (more) {
+          if (!(ok = next_slot(dn))) break;
+          issue_dp(dn);
+        }
+        qs = qn;
+        ds = dn;
       }
-      if (ok && (ok = issue_acc(n_q - 1))) mma_commit(bar(O_FULL));
+      if (ok) mma_commit(bar(O_FULL));
     }
     if (!ok) {
       mma_commit(bar(DRAIN));
@@ -570,6 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (i + 1 < n_q) col_vals(i + 1, nl2, nd);
+      // phase A: P^T from S^T, kept in fp32 registers, written as bf16 over S^T
       ok = __all_sync(0xffffffffu, wait_one(bar(S_FULL), sf_ph, kSiteK | 5));
       if (!ok) break;
       sf_ph ^= 1;
@@ -578,52 +605,71 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the tile needs the causal mask when some (key, query) pair is hidden
       const bool masked_tile = p.causal && __any_sync(0xffffffffu, key > qb + off);
       const bool need_mask = masked_tile || __any_sync(0xffffffffu, !key_ok);
-#pragma unroll 1
-      for (int ch = 2 * hh; ch < 2 * hh + 2; ++ch) {
-        uint32_t s[32], dp[32], pk[16], gk[16];
-        tmem_ld_x32_nowait(tS + 32 * ch, s);  // both loads in flight, one wait
-        tmem_ld_x32_nowait(tDP + 32 * ch, dp);
-        tmem_wait_ld_dep32(s);
-        tmem_wait_ld_dep32(dp);
-        const float4* cl4 = reinterpret_cast<const float4*>(cl + 32 * (ch & 1));
-        const float4* cd4 = reinterpret_cast<const float4*>(cl + kTile / 2 + 32 * (ch & 1));
+      float pr[2][32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int ch = 2 * hh + c;
+        uint32_t sv[32], pk[16];
+        tmem_ld_x32(tS + 32 * ch, sv);
+        const float4* cl4 = reinterpret_cast<const float4*>(cl + 32 * c);
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 l4 = cl4[e4], d4 = cd4[e4];  // -lse2, -D of four columns
+          const float4 l4 = cl4[e4];  // -lse2 of four columns
           const int e = 4 * e4;
-          float x[4], pr[4], t[4], gr[4];
-          fma2(x[0], x[1], __uint_as_float(s[e]), __uint_as_float(s[e + 1]), sl2, sl2, l4.x, l4.y);
-          fma2(x[2], x[3], __uint_as_float(s[e + 2]), __uint_as_float(s[e + 3]), sl2, sl2, l4.z, l4.w);
+          float x[4];
+          fma2(x[0], x[1], __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), sl2, sl2, l4.x, l4.y);
+          fma2(x[2], x[3], __uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3]), sl2, sl2, l4.z, l4.w);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) pr[u] = ex2(x[u]);
+          for (int u = 0; u < 4; ++u) pr[c][e + u] = ex2(x[u]);
           if (need_mask) {
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-              if (!key_ok || (masked_tile && key > qb + 32 * ch + e + u + off)) pr[u] = 0.f;
+              if (!key_ok || (masked_tile && key > qb + 32 * ch + e + u + off)) pr[c][e + u] = 0.f;
           }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) t[u] = __uint_as_float(dp[e + u]);
-          add2(t[0], t[1], d4.x, d4.y);  // dP - D
-          add2(t[2], t[3], d4.z, d4.w);
-          fma2(gr[0], gr[1], t[0], t[1], pr[0], pr[1], 0.f, 0.f);
-          fma2(gr[2], gr[3], t[2], t[3], pr[2], pr[3], 0.f, 0.f);
-          __nv_bfloat162 a0 = __floats2bfloat162_rn(pr[0], pr[1]);
-          __nv_bfloat162 a1 = __floats2bfloat162_rn(pr[2], pr[3]);
-          __nv_bfloat162 g0 = __floats2bfloat162_rn(gr[0], gr[1]);
-          __nv_bfloat162 g1 = __floats2bfloat162_rn(gr[2], gr[3]);
-          pk[2 * e4] = *reinterpret_cast<uint32_t*>(&a0);
-          pk[2 * e4 + 1] = *reinterpret_cast<uint32_t*>(&a1);
-          gk[2 * e4] = *reinterpret_cast<uint32_t*>(&g0);
-          gk[2 * e4 + 1] = *reinterpret_cast<uint32_t*>(&g1);
         }
-        // P^T and dS^T over this half's S^T and dP^T columns, already read
-        tmem_st_x16_nowait(tS + 64 * hh + 16 * (ch & 1), pk);
-        tmem_st_x16_nowait(tDP + 64 * hh + 16 * (ch & 1), gk);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(pr[c][2 * e], pr[c][2 * e + 1]);
+          pk[e] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+        tmem_st_x16_nowait(tS + 64 * hh + 16 * c, pk);  // over this half's S^T, already read
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(P_FULL));
+      // phase B: dS^T = P^T (dP^T - D), written as bf16 over dP^T
+      ok = __all_sync(0xffffffffu, wait_one(bar(DP_FULL), sf_ph ^ 1, kSiteK | 8));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int ch = 2 * hh + c;
+        uint32_t dp[32], gk[16];
+        tmem_ld_x32(tDP + 32 * ch, dp);
+        const float4* cd4 = reinterpret_cast<const float4*>(cl + kTile / 2 + 32 * c);
+#pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 d4 = cd4[e4];  // -D of four columns
+          const int e = 4 * e4;
+          float t[4], g[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) t[u] = __uint_as_float(dp[e + u]);
+          add2(t[0], t[1], d4.x, d4.y);  // dP - D
+          add2(t[2], t[3], d4.z, d4.w);
+          fma2(g[0], g[1], t[0], t[1], pr[c][e], pr[c][e + 1], 0.f, 0.f);
+          fma2(g[2], g[3], t[2], t[3], pr[c][e + 2], pr[c][e + 3], 0.f, 0.f);
+          __nv_bfloat162 g0 = __floats2bfloat162_rn(g[0], g[1]);
+          __nv_bfloat162 g1 = __floats2bfloat162_rn(g[2], g[3]);
+          gk[2 * e4] = *reinterpret_cast<uint32_t*>(&g0);
+          gk[2 * e4 + 1] = *reinterpret_cast<uint32_t*>(&g1);
+        }
+        tmem_st_x16_nowait(tDP + 64 * hh + 16 * c, gk);  // over this half's dP^T, already read
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(DS_FULL));
     }
     if (ok) ok = __all_sync(0xffffffffu, wait_one(bar(O_FULL), 0, kSiteK | 6));
     if (ok) {
