@@ -67,7 +67,8 @@ enum Bar : uint32_t {
   O_FULL = P_FULL + 1,
   DRAIN = O_FULL + 1,
   DP_FULL = DRAIN + 1,   // dK/dV kernel: dP^T ready (S_FULL then only S^T)
-  DS_FULL = DP_FULL + 1, // dK/dV kernel: dS^T written
+  DS_FULL = DP_FULL + 1, // dS (dS^T) written
+  S_FULL1 = DS_FULL + 1, // dQ kernel: the second S buffer ready
   NUM_BARS
 };
 constexpr uint32_t kSmemTmemSlot = kSmemBar + 8 * NUM_BARS;
@@ -204,7 +205,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(RING_EMPTY + s), 1);
     }
     mbar_init(bar(S_FULL), 1);
-    mbar_init(bar(P_FULL), 8);
+    mbar_init(bar(S_FULL1), 1);
+    mbar_init(bar(DP_FULL), 1);
+    mbar_init(bar(DS_FULL), 8);
     mbar_init(bar(O_FULL), 1);
     mbar_init(bar(DRAIN), 1);
     fence_mbar_init();
@@ -254,53 +257,73 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------- MMA issuer
+    // S is double-buffered (TMEM columns 0 and 384): order per key tile j is
+    // S_{j+1} | dQ += dS_j K_j (after dS_j) | dP_{j+1}, so S_{j+1} runs while
+    // the element-wise warps work on tile j.  Every product that overwrites a
+    // TMEM region is issued after the product that reads it.
     const uint64_t dKm = sdesc_sw128(0, 16, 1024);      // K-major template
     const uint64_t dMN = sdesc_sw128(0, 16384, 1024);   // MN-major template
     bool ok = wait_one(bar(RES_FULL), 0, kSiteQ | 2);
-    uint32_t slot = 0, ph = 0, pf_ph = 0;
-    uint32_t k_prev = 0;  // ring slot of K_{j-1}
+    uint32_t slot = 0, ph = 0, df_ph = 0;
     if (ok) {
       tc_fence_after();
       const uint64_t qdesc = dKm + (sQ >> 4), dodesc = dKm + (sDO >> 4);
-      // dQ += dS_{j-1} K_{j-1}, once the softmax warps have written dS
-      auto issue_dq = [&](int jj) -> bool {
-        if (!wait_one(bar(P_FULL), pf_ph, kSiteQ | 3)) return false;
-        pf_ph ^= 1;
-        tc_fence_after();
-        const uint64_t kdesc = dMN + ((sRing + k_prev * kTileBytes) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tbase + kTmemAcc0, tbase + kTmemS + tmem_half_col(kk), kdesc + ((kk * 2048) >> 4),
-                 kIdescKMN, (jj > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(RING_EMPTY + k_prev));  // K_{j-1} is free after this product
-        return true;
+      auto next_slot = [&](uint32_t& s_out) -> bool {  // ring slots in fill order
+        s_out = slot;
+        const bool r = wait_one(bar(RING_FULL + slot), ph, kSiteQ | 4);
+        if (++slot == kSlots) { slot = 0; ph ^= 1; }
+        return r;
       };
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const uint32_t ks = slot;
-        if (!(ok = wait_one(bar(RING_FULL + ks), ph, kSiteQ | 4))) break;
-        if (++slot == kSlots) { slot = 0; ph ^= 1; }
-        const uint32_t vs = slot;
-        if (!(ok = wait_one(bar(RING_FULL + vs), ph, kSiteQ | 4))) break;
-        if (++slot == kSlots) { slot = 0; ph ^= 1; }
-        if (j > 0 && !(ok = issue_dq(j - 1))) break;
+      auto issue_s = [&](uint32_t ks, int jj) {  // S_jj = Q K_jj^T into buffer jj & 1
         tc_fence_after();
         const uint64_t kdesc = dKm + ((sRing + ks * kTileBytes) >> 4);
-        const uint64_t vdesc = dKm + ((sRing + vs * kTileBytes) >> 4);
+        const uint32_t tsb = tbase + ((jj & 1) ? kTmemAcc1 : kTmemS);
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-          mma_ss(tbase + kTmemS, qdesc + off, kdesc + off, kIdescKK, kk > 0 ? 1u : 0u);
+          mma_ss(tsb, qdesc + off, kdesc + off, kIdescKK, kk > 0 ? 1u : 0u);
         }
+        mma_commit(bar((jj & 1) ? S_FULL1 : S_FULL));
+      };
+      auto issue_dp = [&](uint32_t vs) {  // dP = dO V_j^T; V_j is used by dP_j only
+        tc_fence_after();
+        const uint64_t vdesc = dKm + ((sRing + vs * kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
           mma_ss(tbase + kTmemDP, dodesc + off, vdesc + off, kIdescKK, kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar(S_FULL));
-        mma_commit(bar(RING_EMPTY + vs));  // V_j is used by dP_j only
-        k_prev = ks;
+        mma_commit(bar(DP_FULL));
+        mma_commit(bar(RING_EMPTY + vs));
+      };
+      uint32_t ks = 0, vs = 0;
+      if ((ok = next_slot(ks))) issue_s(ks, 0);
+      if (ok && (ok = next_slot(vs))) issue_dp(vs);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const bool more = j + 1 < n_kv;
+        uint32_t kn = 0;
+        if (more) {
+          if (!(ok = next_slot(kn))) break;
+          issue_s(kn, j + 1);
+        }
+        // dQ += dS_j K_j once the element-wise warps have written dS_j
+        if (!(ok = wait_one(bar(DS_FULL), df_ph, kSiteQ | 3))) break;
+        df_ph ^= 1;
+        tc_fence_after();
+        const uint64_t kdesc = dMN + ((sRing + ks * kTileBytes) >> 4);
+        const uint32_t tsb = tbase + ((j & 1) ? kTmemAcc1 : kTmemS);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tbase + kTmemAcc0, tsb + tmem_half_col(kk), kdesc + ((kk * 2048) >> 4), kIdescKMN,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(RING_EMPTY + ks));  // K_j is free after this product
+        if (more) {
+          if (!(ok = next_slot(vs))) break;
+          issue_dp(vs);
+        }
+        ks = kn;
       }
-      if (ok && (ok = issue_dq(n_kv - 1))) mma_commit(bar(O_FULL));
+      if (ok) mma_commit(bar(O_FULL));
     }
     if (!ok) {  // wait for every MMA already issued before TMEM is released
       mma_commit(bar(DRAIN));
@@ -310,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- P and dS
     const int wq = warp & 3, hh = (warp - 4) >> 2;  // lane quarter, column half
     const uint32_t lane_off = static_cast<uint32_t>(32 * wq) << 16;
-    const uint32_t tS = tbase + lane_off + kTmemS, tDP = tbase + lane_off + kTmemDP;
+    const uint32_t tDP = tbase + lane_off + kTmemDP;
     const int row = q0 + 32 * wq + lane;
     const bool row_ok = row < p.Nq;
     const int64_t grow = static_cast<int64_t>(bh) * p.Nq + (row_ok ? row : 0);
@@ -321,42 +344,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     int limit = L;
     if (p.causal) limit = min(limit, row + 1 + (p.Nk - p.Nq));
     const float sl2 = p.scale_log2;
-    uint32_t sf_ph = 0;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      ok = __all_sync(0xffffffffu, wait_one(bar(S_FULL), sf_ph, kSiteQ | 5));
+      // phase A: P from S_j (buffer j & 1), kept in fp32 registers
+      const uint32_t tSb = tbase + lane_off + ((j & 1) ? kTmemAcc1 : kTmemS);
+      ok = __all_sync(0xffffffffu,
+                      wait_one(bar((j & 1) ? S_FULL1 : S_FULL), (j >> 1) & 1, kSiteQ | 5));
       if (!ok) break;
-      sf_ph ^= 1;
       tc_fence_after();
       const int k0 = j * kTile;
       const bool masked_tile = __any_sync(0xffffffffu, k0 + kTile > limit);
-#pragma unroll 1
-      for (int ch = 2 * hh; ch < 2 * hh + 2; ++ch) {
-        uint32_t s[32], dp[32], pk[16];
-        tmem_ld_x32_nowait(tS + 32 * ch, s);  // both loads in flight, one wait
-        tmem_ld_x32_nowait(tDP + 32 * ch, dp);
-        tmem_wait_ld_dep32(s);
-        tmem_wait_ld_dep32(dp);
+      float pr[2][32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int ch = 2 * hh + c;
+        uint32_t sv[32];
+        tmem_ld_x32(tSb + 32 * ch, sv);
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float x0, x1, t0 = __uint_as_float(dp[e]), t1 = __uint_as_float(dp[e + 1]), g0, g1;
-          fma2(x0, x1, __uint_as_float(s[e]), __uint_as_float(s[e + 1]), sl2, sl2, nlse2, nlse2);
-          float p0 = ex2(x0), p1 = ex2(x1);
+          float x0, x1;
+          fma2(x0, x1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), sl2, sl2, nlse2, nlse2);
+          pr[c][e] = ex2(x0);
+          pr[c][e + 1] = ex2(x1);
           if (masked_tile) {
-            if (k0 + 32 * ch + e >= limit) p0 = 0.f;
-            if (k0 + 32 * ch + e + 1 >= limit) p1 = 0.f;
+            if (k0 + 32 * ch + e >= limit) pr[c][e] = 0.f;
+            if (k0 + 32 * ch + e + 1 >= limit) pr[c][e + 1] = 0.f;
           }
+        }
+      }
+      // phase B: dS = P (dP - D), written as bf16 over this half of S_j
+      ok = __all_sync(0xffffffffu, wait_one(bar(DP_FULL), j & 1, kSiteQ | 7));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int ch = 2 * hh + c;
+        uint32_t dp[32], pk[16];
+        tmem_ld_x32(tDP + 32 * ch, dp);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float t0 = __uint_as_float(dp[e]), t1 = __uint_as_float(dp[e + 1]), g0, g1;
           add2(t0, t1, ndlt, ndlt);  // dP - D
-          fma2(g0, g1, t0, t1, p0, p1, 0.f, 0.f);
+          fma2(g0, g1, t0, t1, pr[c][e], pr[c][e + 1], 0.f, 0.f);
           __nv_bfloat162 h2 = __floats2bfloat162_rn(g0, g1);
           pk[e >> 1] = *reinterpret_cast<uint32_t*>(&h2);
         }
-        tmem_st_x16_nowait(tS + 64 * hh + 16 * (ch & 1), pk);  // dS over this half's S, already read
+        tmem_st_x16_nowait(tSb + 64 * hh + 16 * c, pk);  // over this half's S_j, already read
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(P_FULL));
+      if (lane == 0) mbar_arrive(bar(DS_FULL));
     }
     if (ok) ok = __all_sync(0xffffffffu, wait_one(bar(O_FULL), 0, kSiteQ | 6));
     if (ok) {
