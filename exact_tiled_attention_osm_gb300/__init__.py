@@ -49,6 +49,7 @@ SIGNATURES = {
     "osm_lse_merge": (_I, [_P, _P, _I, _I64, _I, _I, _P, _P, _P]),
     "osm_status_string": (ctypes.c_char_p, [_I]),
     "osm_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint32)]),
+    "osm_selftest_bounded_wait": (_I, [_P]),
     "osm_abi_version": (_I, []),
 }
 
@@ -385,6 +386,15 @@ def lse_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, out_dtype=torch.fl
         _check(lib.osm_lse_merge(o_parts.data_ptr(), lse_parts.data_ptr(), S, rows, d, odt,
                                  o.data_ptr(), lse.data_ptr(), _stream(o_parts)), "osm_lse_merge")
     return o, lse
+
+
+def selftest_bounded_wait(device=None) -> None:
+    """Launch the bounded-wait self-test (a wait that runs out; see osm.h)."""
+    lib = load_library()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _check(lib.osm_selftest_bounded_wait(torch.cuda.current_stream(dev).cuda_stream),
+               "osm_selftest_bounded_wait")
 
 
 def device_status(device=None) -> int:

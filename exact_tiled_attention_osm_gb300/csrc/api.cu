@@ -234,6 +234,10 @@ osm_status osm_lse_merge(const float* o_parts, const float* lse_parts, int S, in
                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
+osm_status osm_selftest_bounded_wait(osm_stream_t stream) {
+  return from_cuda(osm::launch_bounded_wait_selftest(reinterpret_cast<cudaStream_t>(stream)));
+}
+
 osm_status osm_device_status(osm_stream_t stream, uint32_t* word) {
   if (!word) return OSM_ERR_INVALID_VALUE;
   *word = 0;

@@ -611,6 +611,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
+// Self-test of the bounded wait: one thread waits on an mbarrier that nothing
+// arrives at.  The wait gives up after its time limit, records `site` in the
+// error word and returns; the kernel then exits normally.
+__global__ void bounded_wait_selftest_kernel(unsigned int* err, unsigned int site) {
+  __shared__ __align__(8) uint64_t mbar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  const uint32_t b = smem_u32(&mbar);
+  mbar_init(b, 1);
+  fence_mbar_init();
+  wait_bounded(b, 0, reinterpret_cast<volatile int*>(&abort_flag), err, site);
+}
+
 // every query row fully masked (no key at all): O = 0, lse = -inf
 __global__ void attn_empty_kernel(__nv_bfloat16* o, float* lse, int64_t rows) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -699,6 +713,15 @@ cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o
     attn_fwd_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
   else
     attn_fwd_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bounded_wait_selftest(cudaStream_t s) {
+  void* errp = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&errp, attn::g_err_word);
+  if (e != cudaSuccess) return e;
+  attn::bounded_wait_selftest_kernel<<<1, 32, 0, s>>>(static_cast<unsigned int*>(errp),
+                                                      0x7f0000a1u);
   return cudaGetLastError();
 }
 

@@ -340,6 +340,16 @@ const char *osm_status_string(osm_status status);
  */
 osm_status osm_device_status(osm_stream_t stream, uint32_t *word);
 
+/*
+ * osm_selftest_bounded_wait — exercise the failure path of the kernels'
+ * bounded waits: one thread waits on a barrier that nothing completes.  The
+ * wait gives up after its limit (about one second), records the site code
+ * 0x7f0000a1 in the device error word and the kernel exits normally; the next
+ * osm_device_status returns OSM_ERR_TIMEOUT with that word.  The device
+ * context stays usable.  Not a hot-path call; for tests of error reporting.
+ */
+osm_status osm_selftest_bounded_wait(osm_stream_t stream);
+
 /* ABI version of this header (major * 100 + minor). */
 int osm_abi_version(void);
 
