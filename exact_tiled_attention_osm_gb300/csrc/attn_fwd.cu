@@ -418,33 +418,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool masked_tile = __any_sync(0xffffffffu, k0 + kKeys > limit);
         const bool first = !kBounded && __any_sync(0xffffffffu, m_ref == kNegInf);
         if (first) {
-          uint32_t sr[128];
           float mx[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
-          if (masked_tile) {
-            tmem_ld_x128(tS, sr);
+#pragma unroll 1
+          for (int ch = 0; ch < 4; ++ch) {  // 32 columns at a time: a small register peak
+            uint32_t sr[32];
+            tmem_ld_x32(tS + 32 * ch, sr);
+            if (masked_tile) {
 #pragma unroll
-            for (int c = 0; c < 128; ++c)
-              if (k0 + c >= limit) sr[c] = __float_as_uint(kNegInf);
-#pragma unroll
-            for (int c = 0; c < 128; c += 8) {
-              mx[0] = max3(mx[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-              mx[1] = max3(mx[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
-              mx[2] = max3(mx[2], __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
-              mx[3] = max3(mx[3], __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+              for (int c = 0; c < 32; ++c)
+                if (k0 + 32 * ch + c >= limit) sr[c] = __float_as_uint(kNegInf);
             }
-          } else {
-            tmem_ld_x64(tS, *reinterpret_cast<uint32_t(*)[64]>(sr));
-            tmem_ld_x64_nowait(tS + 64, sr + 64);
 #pragma unroll
-            for (int c = 0; c < 64; c += 8) {
-              mx[0] = max3(mx[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-              mx[1] = max3(mx[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
-              mx[2] = max3(mx[2], __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
-              mx[3] = max3(mx[3], __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
-            }
-            tmem_wait_ld_dep64(sr + 64);
-#pragma unroll
-            for (int c = 64; c < 128; c += 8) {
+            for (int c = 0; c < 32; c += 8) {
               mx[0] = max3(mx[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
               mx[1] = max3(mx[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
               mx[2] = max3(mx[2], __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
