@@ -21,7 +21,7 @@ definitions and against the numbers the pages print.
 Every function here is pinned by ``tests/test_oracle_pins.py``; none is
 "parity unpinned".
 
-Readings of points the pages leave open (each one is listed in the design doc):
+Readings of points the pages leave open (the CUDA library takes the same ones):
   * A row whose every score is -inf (a fully masked row) has l = 0; its output
     row is 0 and its log-sum-exp is -inf.  [P3] "Precision" says such a row
     "must be handled explicitly"; this is the finalize of the merge identity
