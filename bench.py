@@ -42,8 +42,8 @@ ATTN_SRC = os.path.join(ROOT, "exact_tiled_attention_osm_gb300", "csrc", "attn_f
 # DRAM traffic of one attention launch on this workload from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
 # source it was captured on (sha256 of attn_fwd.cu); None until captured.
-ATTN_TRAFFIC = {"bytes_per_launch": 1_260_000_000 + 517_210_000,
-                "source_sha256": "64ea4cfc354ecbe3e00559f41436475c4399fb5ec81f12237f1b8259c1c4b6ed"}
+ATTN_TRAFFIC = {"bytes_per_launch": 1_260_000_000 + 517_290_000,
+                "source_sha256": "7c819a0c4a79247439bf59e17fbfd6f36be33891631fc87392cdda43bb676a11"}
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
