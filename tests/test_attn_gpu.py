@@ -215,3 +215,25 @@ def test_full_size_causal_padded(cuda_ok):
         idx = torch.as_tensor(rows, device=o.device)
         check(o[b:b + 1, h:h + 1, idx], lse[b:b + 1, h:h + 1, idx], ro, rl)
     assert torch.all(torch.isfinite(o)) and torch.all(torch.isfinite(lse))
+
+
+def test_long_sequence_causal_padded(cuda_ok):
+    """One head pair with 32768 keys (256 key tiles per work item), causal,
+    key_len 20000 and 32768: sampled rows, including the diagonal tiles' edges
+    and rows past key_len."""
+    B, H, N = 2, 2, 32768
+    case = W.attention(91, B, H, N, N, 128, True, None)
+    case.key_len = torch.tensor([20000, 32768], dtype=torch.int32)
+    o, lse = run(case)
+    rows = np.array([0, 1, 127, 128, 4095, 19999, 20000, 20001, 32767])
+    ro, rl = oracle_of(case, rows=rows)
+    check(o[:, :, rows], lse[:, :, rows], ro, rl)
+
+
+def test_cross_attention_shapes(cuda_ok):
+    """Nq != Nk without a causal mask (cross-attention): 512 queries against
+    16384 keys, and 3000 queries against 200 keys."""
+    for seed, (Nq, Nk) in ((92, (512, 16384)), (93, (3000, 200))):
+        case = W.attention(seed, 1, 2, Nq, Nk, 128, False, (Nk // 2, Nk))
+        o, lse = run(case)
+        check(o, lse, *oracle_of(case))

@@ -154,3 +154,15 @@ def test_full_size_decode(cuda_ok):
                                       W.as_f64(vb[None]), case.scale, False, [int(lens[b])])
         check_bf16(o[b:b + 1], lse[b:b + 1], ro, rl)
     assert torch.all(torch.isfinite(o)) and torch.all(torch.isfinite(lse))
+
+
+def test_very_long_cache(cuda_ok):
+    """One query per head against 262144 keys (16 splits of 16384 keys), key
+    lengths 262144 and 100001."""
+    B, H, Nk = 2, 2, 262144
+    case = W.decode(seed=43, B=B, H=H, Nk=Nk, d=128, len_range=(Nk, Nk), num_splits=16)
+    kl = torch.tensor([Nk, 100001], dtype=torch.int32)
+    o, lse = osm.attn_decode_splitkv(case.q.cuda(), case.k.cuda(), case.v.cuda(), case.scale,
+                                     kl.cuda(), 16)
+    assert osm.device_status() == 0
+    check_bf16(o, lse, *ref_decode(case.q, case.k, case.v, case.scale, kl))
