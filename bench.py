@@ -43,7 +43,7 @@ ATTN_SRC = os.path.join(ROOT, "exact_tiled_attention_osm_gb300", "csrc", "attn_f
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
 # source it was captured on (sha256 of attn_fwd.cu); None until captured.
 ATTN_TRAFFIC = {"bytes_per_launch": 1_260_000_000 + 517_290_000,
-                "source_sha256": "7c819a0c4a79247439bf59e17fbfd6f36be33891631fc87392cdda43bb676a11"}
+                "source_sha256": "371a265626d35bc957ca88c6f39dcf76f346f0e19b8d4a72ef80ba8d97c6058b"}
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 

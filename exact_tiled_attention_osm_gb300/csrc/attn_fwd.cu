@@ -144,8 +144,10 @@ __device__ unsigned int g_err_word;
 // Work-item counters.  Each launch takes the next entry (round robin) and
 // zeroes it on its own stream first, so launches on different streams only
 // share a counter when more than kCounters of them are in flight at once.
+// Launches captured into a CUDA graph keep their entry for every replay, so
+// they draw from a second range that direct launches never use.
 constexpr int kCounters = 1024;
-__device__ unsigned int g_item_counter[kCounters];
+__device__ unsigned int g_item_counter[2 * kCounters];
 
 // kBounded: every row starts from the caller's bound (p.m_init finite), so no
 // tile looks for the maximum and an all-underflow start can lower the reference.
@@ -673,8 +675,14 @@ cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o
   void* ctrp = nullptr;
   e = cudaGetSymbolAddress(&ctrp, g_item_counter);
   if (e != cudaSuccess) return e;
-  static std::atomic<unsigned int> next_counter{0};
-  p.next_item = static_cast<unsigned int*>(ctrp) + next_counter.fetch_add(1) % kCounters;
+  static std::atomic<unsigned int> next_direct{0}, next_captured{0};
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(s, &cap);
+  if (e != cudaSuccess) return e;
+  const unsigned int slot = cap == cudaStreamCaptureStatusNone
+                                ? next_direct.fetch_add(1) % kCounters
+                                : kCounters + next_captured.fetch_add(1) % kCounters;
+  p.next_item = static_cast<unsigned int*>(ctrp) + slot;
   e = cudaMemsetAsync(p.next_item, 0, sizeof(unsigned int), s);
   if (e != cudaSuccess) return e;
   // the shared-memory opt-in is per function and per device

@@ -112,6 +112,10 @@ osm_status osm_softmax_topk(const float *x, int64_t rows, int64_t cols, int k, i
  * "Precision, and what can still go wrong": any bound will do); the kernel
  * moves it only when a term would exceed 2^16 or all terms so far underflow.
  * No score matrix is written to memory.
+ * Work is handed to the thread blocks through a library-owned counter that
+ * the call zeroes on `stream` (a 4-byte memset, then the kernel); calls on
+ * different streams may overlap as long as fewer than 1024 direct calls (and,
+ * separately, 1024 captured-graph launches) are in flight at once.
  *
  *   q     [B, H, Nq, d] bf16;  k, v [B, H, Nk, d] bf16 (read only).
  *   o     [B, H, Nq, d] bf16 (written);  lse [B, H, Nq] fp32 (written).
