@@ -373,7 +373,7 @@ def reduce_max(times: dict, world: int, device) -> dict:
 def profile_case(spec: str, iters: int):
     """Run one operation `iters` times on a given shape (for ncu captures).
 
-    spec: "attn:B,H,N[,causal]" | "attnqk:B,H,N[,causal]" (QK-norm inputs with
+    spec: "attn:B,H,N[,causal][,d64]" | "attnqk:B,H,N[,causal]" (QK-norm inputs with
           their score bound) | "bwd:B,H,N[,causal]" | "softmax:rows,cols"
           | "topk:rows,cols,k"
           | "decode:B,H,Nk[,splits]"
@@ -387,12 +387,13 @@ def profile_case(spec: str, iters: int):
     dev = torch.device("cuda", 0)
     if op == "attn":
         B, H, N = (int(x) for x in parts[:3])
-        causal = len(parts) > 3 and parts[3] == "causal"
-        c = W.attention(4, B, H, N, N, 128, causal, (N // 2, N) if causal else None)
+        causal = "causal" in parts[3:]
+        hd = 64 if "d64" in parts[3:] else 128
+        c = W.attention(4, B, H, N, N, hd, causal, (N // 2, N) if causal else None)
         q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
         kl = c.key_len.to(dev) if c.key_len is not None else None
         run = lambda: osm.attn_fwd(q, k, v, c.scale, causal, kl)
-        work = attn_flops(B, H, N, N, 128, causal, None if kl is None else c.key_len.numpy())
+        work = attn_flops(B, H, N, N, hd, causal, None if kl is None else c.key_len.numpy())
         unit = "TFLOP/s"
     elif op == "attnqk":
         # QK-norm inputs (q, k rows scaled to norm sqrt(d)) with their known

@@ -67,7 +67,7 @@ osm_status attn_fwd_checked(const void* q, const void* k, const void* v, void* o
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return OSM_ERR_INVALID_VALUE;
   if (causal != 0 && causal != 1) return OSM_ERR_INVALID_VALUE;
   if (!(scale > 0.f) || !std::isfinite(scale)) return OSM_ERR_INVALID_VALUE;
-  if (d != 128) return (d > 0) ? OSM_ERR_UNSUPPORTED : OSM_ERR_INVALID_VALUE;
+  if (d != 64 && d != 128) return (d > 0) ? OSM_ERR_UNSUPPORTED : OSM_ERR_INVALID_VALUE;
   if (static_cast<int64_t>(B) * H * Nq == 0) return OSM_OK;
   if (!q || !o || !lse || (Nk > 0 && (!k || !v))) return OSM_ERR_INVALID_VALUE;
   if (!aligned16(q) || !aligned16(o) || !aligned4(lse)) return OSM_ERR_INVALID_VALUE;

@@ -52,12 +52,11 @@ namespace attn {
 
 using namespace ptx;
 
-constexpr int kHeadDim = 128;
 constexpr int kRows = 128;   // query rows per tile (MMA M)
 constexpr int kKeys = 128;   // keys per K/V tile (MMA N of QK^T, K of PV)
 constexpr int kSlots = 4;    // K/V ring slots, one 32 KB tile each
 constexpr int kItemSlots = 4;  // depth of the CTA's queue of work-item numbers
-constexpr uint32_t kTileBytes = kRows * kHeadDim * 2;  // 32768
+constexpr uint32_t kTileBytes = kRows * 128 * 2;  // 32768: a tile slot holds d = 128
 constexpr uint32_t kBoxBytes = 128 * 64 * 2;           // one TMA box: 64 columns x 128 rows
 constexpr int kThreads = 384;
 // A 32-term chunk whose sum stays at or below kSumLimit has no term above it
@@ -98,7 +97,6 @@ constexpr uint32_t kTmemS = 0;
 constexpr uint32_t kTmemO = 256;
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);  // Q, K both K-major
-constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, true);  // V is MN-major
 
 // error-word sites (kernel id 1 in the top byte)
 constexpr unsigned kSite = 0x01000000u;
@@ -151,7 +149,9 @@ __device__ unsigned int g_item_counter[2 * kCounters];
 
 // kBounded: every row starts from the caller's bound (p.m_init finite), so no
 // tile looks for the maximum and an all-underflow start can lower the reference.
-template <bool kBounded>
+// D: the head dimension, 64 or 128 (a 64-column tile uses half of each slot and
+// half of each O~ region; the softmax is the same).
+template <bool kBounded, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -251,8 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             qe_ph ^= 1;
           }
           for (int t = 0; t < 2; ++t) {
-            mbar_arrive_expect_tx(bar(Q_FULL + t), kTileBytes);
-            for (int c = 0; c < 2; ++c)
+            mbar_arrive_expect_tx(bar(Q_FULL + t), kRows * D * 2);
+            for (int c = 0; c < D / 64; ++c)
               tma_load_3d(sQ + t * kTileBytes + c * kBoxBytes, &tm_q, bar(Q_FULL + t), c * 64,
                           it.q0 + t * kRows, it.bh);
           }
@@ -263,9 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; ok && j < it.n_kv; ++j) {
             for (int kv = 0; kv < 2; ++kv) {
               if (!(ok = wait_one(bar(KV_EMPTY + slot), ph ^ 1, kSite | 2))) break;
-              mbar_arrive_expect_tx(bar(KV_FULL + slot), kTileBytes);
+              mbar_arrive_expect_tx(bar(KV_FULL + slot), kKeys * D * 2);
               const CUtensorMap* tm = kv ? &tm_v : &tm_k;
-              for (int c = 0; c < 2; ++c)
+              for (int c = 0; c < D / 64; ++c)
                 tma_load_3d(sKV + slot * kTileBytes + c * kBoxBytes, tm, bar(KV_FULL + slot),
                             c * 64, j * kKeys, it.bh);
               fill_mask |= 1u << slot;
@@ -322,7 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kKeys / 16; ++kk) {  // 16 keys = 8 TMEM columns of P, 2 KB of V
             mma_ts(tbase + kTmemO + t * 128, tbase + kTmemS + t * 128 + kk * 8,
-                   vdesc + ((kk * 2048) >> 4), kIdescPV, (!first_pv[t] || kk > 0) ? 1u : 0u);
+                   vdesc + ((kk * 2048) >> 4), idesc_bf16_f32(128, D, true),
+                   (!first_pv[t] || kk > 0) ? 1u : 0u);
           }
           pf_ph[t] ^= 1;
           first_pv[t] = false;
@@ -343,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j > 0 && !(ok = issue_pv(t))) break;
             const uint64_t qdesc = dK + ((sQ + t * kTileBytes) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < kHeadDim / 16; ++kk) {  // 16 columns of d = 32 B of a row
+            for (int kk = 0; kk < D / 16; ++kk) {  // 16 columns of d = 32 B of a row
               const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
               mma_ss(tbase + kTmemS + t * 128, qdesc + off, kdesc + off, kIdescS,
                      kk > 0 ? 1u : 0u);
@@ -395,9 +396,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t orow = static_cast<int64_t>(it.bh) * p.Nq + row;
       if (it.n_kv == 0) {
         if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(p.o + orow * kHeadDim);
+          uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D);
 #pragma unroll
-          for (int i = 0; i < kHeadDim / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+          for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
           p.lse[orow] = kNegInf;
         }
         continue;
@@ -452,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < D / 32; ++c) {
               uint32_t orr[32];
               tmem_ld_x32(tO + 32 * c, orr);
 #pragma unroll
@@ -539,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               // O~'s last update (P V of the previous tile) completed before S
               // (before a row's first P V it holds no value: scaling it is harmless)
 #pragma unroll 1
-              for (int c = 0; c < 4; ++c) {
+              for (int c = 0; c < D / 32; ++c) {
                 uint32_t orr[32];
                 tmem_ld_x32(tO + 32 * c, orr);
 #pragma unroll
@@ -568,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t orr[32];
         tmem_ld_x32(tO + 32 * c, orr);
         if (row_ok) {
@@ -579,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                       __uint_as_float(orr[2 * e + 1]) * inv);
             pk2[e] = *reinterpret_cast<uint32_t*>(&h2);
           }
-          uint4* dst = reinterpret_cast<uint4*>(p.o + orow * kHeadDim + 32 * c);
+          uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D + 32 * c);
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             dst[e] = make_uint4(pk2[4 * e], pk2[4 * e + 1], pk2[4 * e + 2], pk2[4 * e + 3]);
@@ -613,9 +614,9 @@ __global__ void bounded_wait_selftest_kernel(unsigned int* err, unsigned int sit
 }
 
 // every query row fully masked (no key at all): O = 0, lse = -inf
-__global__ void attn_empty_kernel(__nv_bfloat16* o, float* lse, int64_t rows) {
+__global__ void attn_empty_kernel(__nv_bfloat16* o, float* lse, int64_t rows, int d) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i < rows * (kHeadDim / 8)) reinterpret_cast<uint4*>(o)[i] = make_uint4(0, 0, 0, 0);
+  if (i < rows * (d / 8)) reinterpret_cast<uint4*>(o)[i] = make_uint4(0, 0, 0, 0);
   if (i < rows) lse[i] = kNegInf;
 }
 
@@ -634,19 +635,18 @@ cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o
                             bool* tmap_ok) {
   using namespace attn;
   *tmap_ok = true;
-  (void)d;
   const int64_t rows = static_cast<int64_t>(B) * H * Nq;
   if (Nk == 0) {
-    const int64_t n = rows * (kHeadDim / 8);
+    const int64_t n = rows * (d / 8);
     attn_empty_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(
-        static_cast<__nv_bfloat16*>(o), lse, rows);
+        static_cast<__nv_bfloat16*>(o), lse, rows, d);
     return cudaGetLastError();
   }
   CUtensorMap tq, tk, tv;
   const uint64_t BH = static_cast<uint64_t>(B) * H;
-  if (!make_tmap_bf16_3d(&tq, q, kHeadDim, Nq, BH, 64, kRows) ||
-      !make_tmap_bf16_3d(&tk, k, kHeadDim, Nk, BH, 64, kKeys) ||
-      !make_tmap_bf16_3d(&tv, v, kHeadDim, Nk, BH, 64, kKeys)) {
+  if (!make_tmap_bf16_3d(&tq, q, d, Nq, BH, 64, kRows) ||
+      !make_tmap_bf16_3d(&tk, k, d, Nk, BH, 64, kKeys) ||
+      !make_tmap_bf16_3d(&tv, v, d, Nk, BH, 64, kKeys)) {
     *tmap_ok = false;
     return cudaSuccess;
   }
@@ -692,20 +692,30 @@ cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(attr_done & bit)) {
-    e = cudaFuncSetAttribute(attn_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return e;
+    for (const void* fn : {reinterpret_cast<const void*>(attn_fwd_kernel<false, 128>),
+                           reinterpret_cast<const void*>(attn_fwd_kernel<true, 128>),
+                           reinterpret_cast<const void*>(attn_fwd_kernel<false, 64>),
+                           reinterpret_cast<const void*>(attn_fwd_kernel<true, 64>)}) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kSmemBytes));
+      if (e != cudaSuccess) return e;
+    }
     attr_done |= bit;
   }
   const int grid = static_cast<int>(items < sm_count_current_device() ? items
                                                                       : sm_count_current_device());
-  if (std::isfinite(score_bound))
-    attn_fwd_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
-  else
-    attn_fwd_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+  const bool bounded = std::isfinite(score_bound);
+  if (d == 128) {
+    if (bounded)
+      attn_fwd_kernel<true, 128><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+    else
+      attn_fwd_kernel<false, 128><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+  } else {
+    if (bounded)
+      attn_fwd_kernel<true, 64><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+    else
+      attn_fwd_kernel<false, 64><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+  }
   return cudaGetLastError();
 }
 

@@ -119,7 +119,7 @@ osm_status osm_softmax_topk(const float *x, int64_t rows, int64_t cols, int k, i
  *
  *   q     [B, H, Nq, d] bf16;  k, v [B, H, Nk, d] bf16 (read only).
  *   o     [B, H, Nq, d] bf16 (written);  lse [B, H, Nq] fp32 (written).
- *   d     must be 128 (other values return OSM_ERR_UNSUPPORTED).
+ *   d     64 or 128 (other values return OSM_ERR_UNSUPPORTED).
  *   scale finite and > 0 (e.g. 1/sqrt(d)).
  *   causal 0 or 1.
  *   key_len device int32[B] (valid keys per batch entry, clamped to [0, Nk]

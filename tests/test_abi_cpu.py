@@ -107,7 +107,7 @@ def test_attn_validation(lib):
     assert call(lse=None) == osm.OSM_ERR_INVALID_VALUE
     assert call(q=FAKE + 8) == osm.OSM_ERR_INVALID_VALUE
     assert call(B=-1) == osm.OSM_ERR_INVALID_VALUE
-    assert call(d=64) == osm.OSM_ERR_UNSUPPORTED
+    assert call(d=96) == osm.OSM_ERR_UNSUPPORTED
     assert call(d=0) == osm.OSM_ERR_INVALID_VALUE
     assert call(scale=0.0) == osm.OSM_ERR_INVALID_VALUE
     assert call(scale=-1.0) == osm.OSM_ERR_INVALID_VALUE
@@ -132,7 +132,7 @@ def test_bounded_attn_validation(lib):
     assert call(13, float("inf")) == osm.OSM_ERR_INVALID_VALUE
     assert call(13, 1e31) == osm.OSM_ERR_INVALID_VALUE
     assert call(0, None) == osm.OSM_ERR_INVALID_VALUE              # then the usual checks
-    assert call(9, 64) == osm.OSM_ERR_UNSUPPORTED
+    assert call(9, 96) == osm.OSM_ERR_UNSUPPORTED
     assert call(5, 0) == osm.OSM_OK                                 # empty: no-op
 
 

@@ -237,3 +237,31 @@ def test_cross_attention_shapes(cuda_ok):
         case = W.attention(seed, 1, 2, Nq, Nk, 128, False, (Nk // 2, Nk))
         o, lse = run(case)
         check(o, lse, *oracle_of(case))
+
+
+D64_SHAPES = [(1, 1, 1, 1), (1, 2, 65, 65), (2, 1, 127, 129), (1, 2, 300, 300), (1, 1, 257, 1000),
+              (2, 2, 1000, 1000)]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", D64_SHAPES)
+def test_head_dim_64(cuda_ok, shape, causal):
+    """d = 64: one 64-column TMA box per tile, N = 64 P.V products."""
+    B, H, Nq, Nk = shape
+    case = W.attention(sum(shape) + 300 + 7 * causal, B, H, Nq, Nk, 64, causal,
+                       (max(1, Nk // 3), Nk))
+    o, lse = run(case)
+    check(o, lse, *oracle_of(case))
+
+
+def test_head_dim_64_edges_and_bound(cuda_ok):
+    N = 300
+    case = W.attention(95, 4, 2, N, N, 64, True, None)
+    case.key_len = torch.tensor([0, 1, N - 1, N], dtype=torch.int32)
+    o, lse = run(case)
+    check(o, lse, *oracle_of(case))
+    assert torch.all(o[0] == 0) and torch.all(torch.isneginf(lse[0]))
+    ob, lb = osm.attn_fwd(case.q.cuda(), case.k.cuda(), case.v.cuda(), case.scale, True,
+                          case.key_len.cuda(), score_bound=3.0)
+    assert osm.device_status() == 0
+    check(ob, lb, *oracle_of(case))
