@@ -265,3 +265,24 @@ def test_head_dim_64_edges_and_bound(cuda_ok):
                           case.key_len.cuda(), score_bound=3.0)
     assert osm.device_status() == 0
     check(ob, lb, *oracle_of(case))
+
+
+def test_cross_check_torch_sdpa(cuda_ok):
+    """Secondary cross-check (not the oracle): torch's scaled_dot_product_attention
+    on the same bf16 tensors, causal and with a padding mask; both sides round
+    to bf16, so they agree to a few bf16 ulps of O."""
+    import torch.nn.functional as F
+    for causal in (False, True):
+        case = W.attention(96 + causal, 2, 4, 1024, 1024, 128, causal, (600, 1024))
+        q, k, v = case.q.cuda(), case.k.cuda(), case.v.cuda()
+        kl = case.key_len.cuda()
+        o, _ = osm.attn_fwd(q, k, v, case.scale, causal, kl)
+        assert osm.device_status() == 0
+        j = torch.arange(1024, device="cuda")
+        mask = (j[None, :] < kl[:, None])[:, None, None, :]
+        if causal:
+            mask = mask & (j[None, :] <= j[:, None])[None, None]
+        ref = F.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=case.scale)
+        err = (o.float() - ref.float()).abs()
+        assert float(err.max()) <= 2e-2
+        assert float(err.mean()) <= 2e-3
