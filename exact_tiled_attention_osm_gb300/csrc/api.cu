@@ -111,7 +111,7 @@ osm_status osm_attn_bwd(const void* q, const void* k, const void* v, const void*
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return OSM_ERR_INVALID_VALUE;
   if (causal != 0 && causal != 1) return OSM_ERR_INVALID_VALUE;
   if (!(scale > 0.f) || !std::isfinite(scale)) return OSM_ERR_INVALID_VALUE;
-  if (d != 128) return (d > 0) ? OSM_ERR_UNSUPPORTED : OSM_ERR_INVALID_VALUE;
+  if (d != 64 && d != 128) return (d > 0) ? OSM_ERR_UNSUPPORTED : OSM_ERR_INVALID_VALUE;
   if (static_cast<int64_t>(B) * H == 0 || (Nq == 0 && Nk == 0)) return OSM_OK;
   if (Nq > 0 && (!q || !o || !lse || !dout || !dq)) return OSM_ERR_INVALID_VALUE;
   if (Nk > 0 && (!k || !v || !dk || !dv)) return OSM_ERR_INVALID_VALUE;
@@ -128,7 +128,7 @@ osm_status osm_attn_bwd(const void* q, const void* k, const void* v, const void*
   const int64_t tiles = static_cast<int64_t>(B) * H * ((std::max(Nq, Nk) + 127) / 128);
   if (tiles > 0x7fffffffLL) return OSM_ERR_UNSUPPORTED;
   bool tmap_ok = true;
-  cudaError_t e = osm::launch_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, scale,
+  cudaError_t e = osm::launch_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, scale,
                                        causal, key_len, workspace,
                                        reinterpret_cast<cudaStream_t>(stream), &tmap_ok);
   if (!tmap_ok) return OSM_ERR_UNSUPPORTED;

@@ -39,10 +39,9 @@ namespace bwd {
 
 using namespace ptx;
 
-constexpr int kHeadDim = 128;
 constexpr int kTile = 128;   // rows of every tile (query or key)
 constexpr int kSlots = 4;    // streamed 32 KB tiles in flight
-constexpr uint32_t kTileBytes = kTile * kHeadDim * 2;  // 32768
+constexpr uint32_t kTileBytes = kTile * 128 * 2;  // 32768: a slot holds a d = 128 tile
 constexpr uint32_t kBoxBytes = 128 * 64 * 2;           // one TMA box: 64 columns x 128 rows
 constexpr int kThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 4-11 element-wise
 // The element-wise warps: two per TMEM lane quarter, warp 4 + q + 4h takes
@@ -81,7 +80,6 @@ constexpr uint32_t kSmemBytes = kSmemCol + 8 * kColFloats * 4 + 1024;
 constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemAcc0 = 256, kTmemAcc1 = 384;
 
 constexpr uint32_t kIdescKK = idesc_bf16_f32(128, 128, false);  // both operands K-major
-constexpr uint32_t kIdescKMN = idesc_bf16_f32(128, 128, true);  // B MN-major
 
 constexpr unsigned kSiteQ = 0x02000000u;   // error-word sites of the dQ kernel
 constexpr unsigned kSiteK = 0x03000000u;   // ... and of the dK/dV kernel
@@ -131,26 +129,29 @@ __device__ __forceinline__ void store_row_bf16(uint32_t t_acc, float mul, __nv_b
   }
 }
 
+template <int D>
 __device__ __forceinline__ void zero_row_bf16(__nv_bfloat16* dst) {
   uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-  for (int e = 0; e < kHeadDim / 8; ++e) d4[e] = make_uint4(0, 0, 0, 0);
+  for (int e = 0; e < D / 8; ++e) d4[e] = make_uint4(0, 0, 0, 0);
 }
 
 __device__ unsigned int g_bwd_err;
 
 // ------------------------------------------------------------------ D
+template <int D>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
                                                         const __nv_bfloat16* __restrict__ dout,
                                                         float* __restrict__ delta, int64_t rows) {
-  // 16 lanes per row, 8 columns (one 16-byte load of each tensor) per lane
+  // D/8 lanes per row, 8 columns (one 16-byte load of each tensor) per lane
+  constexpr int kLanes = D / 8;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t row = t >> 4;
-  const int sl = threadIdx.x & 15;
+  const int64_t row = t / kLanes;
+  const int sl = threadIdx.x % kLanes;
   float acc = 0.f;
   if (row < rows) {
-    const uint4 a = reinterpret_cast<const uint4*>(o + row * kHeadDim)[sl];
-    const uint4 g = reinterpret_cast<const uint4*>(dout + row * kHeadDim)[sl];
+    const uint4 a = reinterpret_cast<const uint4*>(o + row * D)[sl];
+    const uint4 g = reinterpret_cast<const uint4*>(dout + row * D)[sl];
     const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wg[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -159,12 +160,13 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __r
     }
   }
 #pragma unroll
-  for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (row < rows && sl == 0) delta[row] = acc;
 }
 
 // ------------------------------------------------------------------ dQ
-// Item = (bh, query tile); causal items longest first.
+// Item = (bh, query tile); causal items longest first.  D: head dimension.
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -192,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (n_kv == 0) {  // no visible key for any row of the tile: dQ = 0
     if (warp >= 4 && warp < 8) {
       const int row = q0 + 32 * (warp - 4) + lane;
-      if (row < p.Nq) zero_row_bf16(p.dq + (static_cast<int64_t>(bh) * p.Nq + row) * kHeadDim);
+      if (row < p.Nq) zero_row_bf16<D>(p.dq + (static_cast<int64_t>(bh) * p.Nq + row) * D);
     }
     return;
   }
@@ -230,8 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
     prefetch_tmap(&tm_do);
-    mbar_arrive_expect_tx(bar(RES_FULL), 2 * kTileBytes);
-    for (int c = 0; c < 2; ++c) {
+    mbar_arrive_expect_tx(bar(RES_FULL), 2 * kTile * D * 2);
+    for (int c = 0; c < D / 64; ++c) {
       tma_load_3d(sQ + c * kBoxBytes, &tm_q, bar(RES_FULL), c * 64, q0, bh);
       tma_load_3d(sDO + c * kBoxBytes, &tm_do, bar(RES_FULL), c * 64, q0, bh);
     }
@@ -240,9 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; ok && j < n_kv; ++j) {
       for (int kv = 0; kv < 2; ++kv) {  // K_j then V_j
         if (!(ok = wait_one(bar(RING_EMPTY + slot), ph ^ 1, kSiteQ | 1))) break;
-        mbar_arrive_expect_tx(bar(RING_FULL + slot), kTileBytes);
+        mbar_arrive_expect_tx(bar(RING_FULL + slot), kTile * D * 2);
         const CUtensorMap* tm = kv ? &tm_v : &tm_k;
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < D / 64; ++c)
           tma_load_3d(sRing + slot * kTileBytes + c * kBoxBytes, tm, bar(RING_FULL + slot), c * 64,
                       j * kTile, bh);
         fill_mask |= 1u << slot;
@@ -279,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t kdesc = dKm + ((sRing + ks * kTileBytes) >> 4);
         const uint32_t tsb = tbase + ((jj & 1) ? kTmemAcc1 : kTmemS);
 #pragma unroll
-        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
           mma_ss(tsb, qdesc + off, kdesc + off, kIdescKK, kk > 0 ? 1u : 0u);
         }
@@ -289,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint64_t vdesc = dKm + ((sRing + vs * kTileBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
           mma_ss(tbase + kTmemDP, dodesc + off, vdesc + off, kIdescKK, kk > 0 ? 1u : 0u);
         }
@@ -314,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tsb = tbase + ((j & 1) ? kTmemAcc1 : kTmemS);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tbase + kTmemAcc0, tsb + tmem_half_col(kk), kdesc + ((kk * 2048) >> 4), kIdescKMN,
+          mma_ts(tbase + kTmemAcc0, tsb + tmem_half_col(kk), kdesc + ((kk * 2048) >> 4), idesc_bf16_f32(128, D, true),
                  (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(RING_EMPTY + ks));  // K_j is free after this product
         if (more) {
@@ -400,8 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       tc_fence_after();
       store_row_bf16(tbase + lane_off + kTmemAcc0, p.scale,
-                     p.dq + (static_cast<int64_t>(bh) * p.Nq + row) * kHeadDim, row_ok, 2 * hh,
-                     2 * hh + 2);
+                     p.dq + (static_cast<int64_t>(bh) * p.Nq + row) * D, row_ok,
+                     hh * (D / 64), (hh + 1) * (D / 64));
     }
   }
   tc_fence_before();
@@ -412,7 +414,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ dK, dV
 // Item = (bh, key tile); causal items longest first (early key tiles are
-// seen by the most query tiles).
+// seen by the most query tiles).  D: head dimension.
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
@@ -442,9 +445,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp >= 4 && warp < 8) {
       const int key = k0 + 32 * (warp - 4) + lane;
       if (key < p.Nk) {
-        const int64_t g = (static_cast<int64_t>(bh) * p.Nk + key) * kHeadDim;
-        zero_row_bf16(p.dk + g);
-        zero_row_bf16(p.dv + g);
+        const int64_t g = (static_cast<int64_t>(bh) * p.Nk + key) * D;
+        zero_row_bf16<D>(p.dk + g);
+        zero_row_bf16<D>(p.dv + g);
       }
     }
     return;
@@ -483,8 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
     prefetch_tmap(&tm_do);
-    mbar_arrive_expect_tx(bar(RES_FULL), 2 * kTileBytes);
-    for (int c = 0; c < 2; ++c) {
+    mbar_arrive_expect_tx(bar(RES_FULL), 2 * kTile * D * 2);
+    for (int c = 0; c < D / 64; ++c) {
       tma_load_3d(sK + c * kBoxBytes, &tm_k, bar(RES_FULL), c * 64, k0, bh);
       tma_load_3d(sV + c * kBoxBytes, &tm_v, bar(RES_FULL), c * 64, k0, bh);
     }
@@ -494,9 +497,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qrow = (qt_first + i) * kTile;
       for (int t = 0; t < 2; ++t) {  // Q_i then dO_i
         if (!(ok = wait_one(bar(RING_EMPTY + slot), ph ^ 1, kSiteK | 1))) break;
-        mbar_arrive_expect_tx(bar(RING_FULL + slot), kTileBytes);
+        mbar_arrive_expect_tx(bar(RING_FULL + slot), kTile * D * 2);
         const CUtensorMap* tm = t ? &tm_do : &tm_q;
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < D / 64; ++c)
           tma_load_3d(sRing + slot * kTileBytes + c * kBoxBytes, tm, bar(RING_FULL + slot), c * 64,
                       qrow, bh);
         fill_mask |= 1u << slot;
@@ -532,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint64_t qdesc = dKm + ((sRing + qs * kTileBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t o16 = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
           mma_ss(tbase + kTmemS, kdesc + o16, qdesc + o16, kIdescKK, kk > 0 ? 1u : 0u);
         }
@@ -542,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint64_t dodesc = dKm + ((sRing + ds * kTileBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t o16 = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
           mma_ss(tbase + kTmemDP, vdesc + o16, dodesc + o16, kIdescKK, kk > 0 ? 1u : 0u);
         }
@@ -562,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           mma_ts(tbase + kTmemAcc0, tbase + kTmemS + tmem_half_col(kk), dod + ((kk * 2048) >> 4),
-                 kIdescKMN, (i > 0 || kk > 0) ? 1u : 0u);
+                 idesc_bf16_f32(128, D, true), (i > 0 || kk > 0) ? 1u : 0u);
         if (more) {
           if (!(ok = next_slot(qn))) break;
           issue_s(qn);
@@ -575,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           mma_ts(tbase + kTmemAcc1, tbase + kTmemDP + tmem_half_col(kk), qd + ((kk * 2048) >> 4),
-                 kIdescKMN, (i > 0 || kk > 0) ? 1u : 0u);
+                 idesc_bf16_f32(128, D, true), (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(RING_EMPTY + qs));
         mma_commit(bar(RING_EMPTY + ds));
         if (more) {
@@ -713,11 +716,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       tc_fence_after();
       const bool st_ok = key < p.Nk;
-      const int64_t g = (static_cast<int64_t>(bh) * p.Nk + (st_ok ? key : 0)) * kHeadDim;
+      const int64_t g = (static_cast<int64_t>(bh) * p.Nk + (st_ok ? key : 0)) * D;
       if (hh == 0)
-        store_row_bf16(tbase + lane_off + kTmemAcc0, 1.f, p.dv + g, st_ok);
+        store_row_bf16(tbase + lane_off + kTmemAcc0, 1.f, p.dv + g, st_ok, 0, D / 32);
       else
-        store_row_bf16(tbase + lane_off + kTmemAcc1, p.scale, p.dk + g, st_ok);
+        store_row_bf16(tbase + lane_off + kTmemAcc1, p.scale, p.dk + g, st_ok, 0, D / 32);
     }
   }
   tc_fence_before();
@@ -734,7 +737,7 @@ size_t attn_bwd_workspace_bytes(int B, int H, int Nq) {
 
 cudaError_t launch_attn_bwd(const void* q, const void* k, const void* v, const void* o,
                             const float* lse, const void* dout, void* dq, void* dk, void* dv,
-                            int B, int H, int Nq, int Nk, float scale, int causal,
+                            int B, int H, int Nq, int Nk, int d, float scale, int causal,
                             const int32_t* key_len, void* workspace, cudaStream_t s,
                             bool* tmap_ok) {
   using namespace bwd;
@@ -743,17 +746,23 @@ cudaError_t launch_attn_bwd(const void* q, const void* k, const void* v, const v
   const int64_t qrows = BH * Nq;
   float* delta = static_cast<float*>(workspace);
   if (Nq > 0) {
-    bwd_delta_kernel<<<static_cast<unsigned>((qrows * 16 + 255) / 256), 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), delta,
-        qrows);
+    const unsigned nb = static_cast<unsigned>((qrows * (d / 8) + 255) / 256);
+    if (d == 128)
+      bwd_delta_kernel<128><<<nb, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
+                                               static_cast<const __nv_bfloat16*>(dout), delta,
+                                               qrows);
+    else
+      bwd_delta_kernel<64><<<nb, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
+                                              static_cast<const __nv_bfloat16*>(dout), delta,
+                                              qrows);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   CUtensorMap tq, tk, tv, tdo;
-  if (!make_tmap_bf16_3d(&tq, q, kHeadDim, Nq, BH, 64, kTile) ||
-      !make_tmap_bf16_3d(&tk, k, kHeadDim, Nk, BH, 64, kTile) ||
-      !make_tmap_bf16_3d(&tv, v, kHeadDim, Nk, BH, 64, kTile) ||
-      !make_tmap_bf16_3d(&tdo, dout, kHeadDim, Nq, BH, 64, kTile)) {
+  if (!make_tmap_bf16_3d(&tq, q, d, Nq, BH, 64, kTile) ||
+      !make_tmap_bf16_3d(&tk, k, d, Nk, BH, 64, kTile) ||
+      !make_tmap_bf16_3d(&tv, v, d, Nk, BH, 64, kTile) ||
+      !make_tmap_bf16_3d(&tdo, dout, d, Nq, BH, 64, kTile)) {
     *tmap_ok = false;
     return cudaSuccess;
   }
@@ -783,31 +792,39 @@ cudaError_t launch_attn_bwd(const void* q, const void* k, const void* v, const v
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(attr_done & bit)) {
-    e = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return e;
+    for (const void* fn : {reinterpret_cast<const void*>(bwd_dq_kernel<128>),
+                           reinterpret_cast<const void*>(bwd_dkdv_kernel<128>),
+                           reinterpret_cast<const void*>(bwd_dq_kernel<64>),
+                           reinterpret_cast<const void*>(bwd_dkdv_kernel<64>)}) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kSmemBytes));
+      if (e != cudaSuccess) return e;
+    }
     attr_done |= bit;
   }
   if (Nk > 0 && Nq > 0) {
-    bwd_dkdv_kernel<<<static_cast<unsigned>(BH * p.n_kt), kThreads, kSmemBytes, s>>>(tq, tk, tv,
-                                                                                   tdo, p);
+    const unsigned g = static_cast<unsigned>(BH * p.n_kt);
+    if (d == 128)
+      bwd_dkdv_kernel<128><<<g, kThreads, kSmemBytes, s>>>(tq, tk, tv, tdo, p);
+    else
+      bwd_dkdv_kernel<64><<<g, kThreads, kSmemBytes, s>>>(tq, tk, tv, tdo, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   } else if (Nk > 0) {  // no query: dK = dV = 0
-    e = cudaMemsetAsync(dk, 0, static_cast<size_t>(BH) * Nk * kHeadDim * 2, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, static_cast<size_t>(BH) * Nk * kHeadDim * 2, s);
+    e = cudaMemsetAsync(dk, 0, static_cast<size_t>(BH) * Nk * d * 2, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, static_cast<size_t>(BH) * Nk * d * 2, s);
     if (e != cudaSuccess) return e;
   }
   if (Nq > 0) {
     if (Nk > 0) {
-      bwd_dq_kernel<<<static_cast<unsigned>(BH * p.n_qt), kThreads, kSmemBytes, s>>>(tq, tk, tv,
-                                                                                   tdo, p);
+      const unsigned g = static_cast<unsigned>(BH * p.n_qt);
+      if (d == 128)
+        bwd_dq_kernel<128><<<g, kThreads, kSmemBytes, s>>>(tq, tk, tv, tdo, p);
+      else
+        bwd_dq_kernel<64><<<g, kThreads, kSmemBytes, s>>>(tq, tk, tv, tdo, p);
       e = cudaGetLastError();
     } else {  // no key: dQ = 0
-      e = cudaMemsetAsync(dq, 0, static_cast<size_t>(BH) * Nq * kHeadDim * 2, s);
+      e = cudaMemsetAsync(dq, 0, static_cast<size_t>(BH) * Nq * d * 2, s);
     }
   }
   return e;

@@ -30,7 +30,7 @@ cudaError_t launch_bounded_wait_selftest(cudaStream_t s);
 size_t attn_bwd_workspace_bytes(int B, int H, int Nq);
 cudaError_t launch_attn_bwd(const void* q, const void* k, const void* v, const void* o,
                             const float* lse, const void* dout, void* dq, void* dk, void* dv,
-                            int B, int H, int Nq, int Nk, float scale, int causal,
+                            int B, int H, int Nq, int Nk, int d, float scale, int causal,
                             const int32_t* key_len, void* workspace, cudaStream_t s,
                             bool* tmap_ok);
 cudaError_t read_and_clear_bwd_error(uint32_t* word);

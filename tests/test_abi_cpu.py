@@ -155,7 +155,7 @@ def test_bwd_validation(lib):
     assert call(dk=None) == osm.OSM_ERR_INVALID_VALUE
     assert call(lse=FAKE + 2) == osm.OSM_ERR_INVALID_VALUE
     assert call(dq=FAKE + 8) == osm.OSM_ERR_INVALID_VALUE
-    assert call(d=64) == osm.OSM_ERR_UNSUPPORTED
+    assert call(d=96) == osm.OSM_ERR_UNSUPPORTED
     assert call(scale=0.0) == osm.OSM_ERR_INVALID_VALUE
     assert call(causal=3) == osm.OSM_ERR_INVALID_VALUE
     assert call(ws=None) == osm.OSM_ERR_INVALID_VALUE

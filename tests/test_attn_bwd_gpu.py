@@ -24,11 +24,11 @@ pytestmark = pytest.mark.gpu
 _DO = 7  # tensor id of dO within a case's seed
 
 
-def make_case(seed, B, H, Nq, Nk, causal, len_range=None, key_len=None):
-    c = W.attention(seed, B, H, Nq, Nk, 128, causal, len_range)
+def make_case(seed, B, H, Nq, Nk, causal, len_range=None, key_len=None, d=128):
+    c = W.attention(seed, B, H, Nq, Nk, d, causal, len_range)
     if key_len is not None:
         c.key_len = torch.tensor(key_len, dtype=torch.int32)
-    do = W.to_bf16(W.normal_bhnd(seed, _DO, B, H, Nq, 128))
+    do = W.to_bf16(W.normal_bhnd(seed, _DO, B, H, Nq, d))
     kl = c.key_len.numpy() if c.key_len is not None else None
     o64, lse64 = oracle.attention_ref(W.as_f64(c.q), W.as_f64(c.k), W.as_f64(c.v), c.scale,
                                       causal, kl)
@@ -128,3 +128,22 @@ def test_full_size_causal_padded_sampled_heads(cuda_ok):
                          c.key_len[b:b + 1])
         check(sub, do[b:b + 1, :1], o[b:b + 1, :1], lse[b:b + 1, :1],
               tuple(g[b:b + 1, :1] for g in got))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", [(1, 2, 65, 65), (2, 1, 127, 129), (1, 2, 300, 300),
+                                   (1, 1, 1000, 257), (2, 2, 513, 513)])
+def test_head_dim_64(cuda_ok, shape, causal):
+    B, H, Nq, Nk = shape
+    c, do, o, lse = make_case(sum(shape) + 400 + 9 * causal, B, H, Nq, Nk, causal,
+                              (max(1, Nk // 3), Nk), d=64)
+    check(c, do, o, lse, run_gpu(c, do, o, lse))
+
+
+def test_head_dim_64_key_len_edges(cuda_ok):
+    N = 300
+    c, do, o, lse = make_case(36, 4, 2, N, N, True, key_len=[0, 1, N - 1, N], d=64)
+    got = run_gpu(c, do, o, lse)
+    check(c, do, o, lse, got)
+    for g in got:
+        assert torch.all(g[0] == 0)
