@@ -1,25 +1,29 @@
-// softmax_topk.cu — fused online softmax + top-k of every row, one read of x.
+// softmax_topk.cu — fused online softmax + top-k of every row; x comes from
+// HBM once.
 //
 // "Online softmax" (zerotofrontier.app), the `softmax_topk` exercise after
 // "Precision, and what can still go wrong", and the reading list's Milakov &
 // Gimelshein entry: the indices of a row's k largest scores together with
-// their softmax probabilities, from one pass over the row.  Each thread keeps
-// the online normaliser (m, l) of its elements ("The recurrence, and a proof
-// that it is right") and a sorted list of its k best (value, index) pairs;
-// both kinds of summary merge exactly in any grouping ("Merging partial
-// results"), so the row's result is assembled warp -> CTA -> thread-block
-// cluster.  Order: larger value first, equal values by smaller index, so the
-// result is unique.  Probabilities are exp(x_i - M) / L with the row's (M, L).
+// their softmax probabilities, fused with the normaliser.  Threads keep the
+// online normaliser (m, l) of their elements ("The recurrence, and a proof
+// that it is right") and warps keep sorted lists of their best (value, index)
+// pairs; both kinds of summary merge exactly in any grouping ("Merging
+// partial results"), so the row's result is assembled warp -> CTA ->
+// thread-block cluster.  Order: larger value first, equal values by smaller
+// index, so the result is unique.  Probabilities are exp(x_i - M) / L with
+// the row's (M, L).
 //
 // GB300 mapping: one cluster of nct CTAs (256 threads each) per row; CTA r of
 // the cluster streams a contiguous slice of the row with 16-byte loads, four
 // in flight per thread, twice: the first pass forms (m, l) and each thread's
-// maximum, whose k-th largest within the warp is a threshold every top-k
-// entry reaches; the second pass (served mostly from L2, the slice was just
-// read) merges only entries that beat it into the warp's running list.  Lists
-// merge by k rounds of a warp-wide arg-max over the lanes' list heads; the
-// CTA's lists meet in shared memory and the cluster's in CTA 0 through
-// distributed shared memory.  HBM-bound: 4 bytes read per element once from
+// maximum, whose k-th largest within the warp (within the CTA for k > 16) is
+// a threshold every top-k entry reaches; the second pass (served mostly from
+// L2, the slice was just read) merges only entries that beat the warp's filter
+// into the warp's running list of 32 pairs, one per lane, by bitonic sort and
+// merge, and tightens the filter to the list's k-th entry.  The CTA's lists
+// meet in warp 0 through shared memory and the cluster's in CTA 0 through
+// distributed shared memory, again by bitonic merges.  K = 1 needs one pass
+// (each thread's arg-max).  HBM-bound: 4 bytes read per element once from
 // HBM, 8 bytes written per output entry.
 #include <cuda_runtime.h>
 

@@ -73,22 +73,25 @@ osm_status osm_softmax_rows(const float *x, float *y, int64_t rows, int64_t cols
 
 /*
  * osm_softmax_topk — the k largest entries of every row of an fp32 matrix and
- * their softmax probabilities, from one read of the row.
+ * their softmax probabilities, fused: the row comes from HBM once.
  *
  * Defines ([P3] the `softmax_topk` exercise after "Precision, and what can
  * still go wrong", Milakov & Gimelshein's fused softmax + top-k): for row r,
  * idx[r, 0..k-1] are the columns of the k largest x[r, :], in the order
  * larger value first, equal values by smaller column (a total order, so the
  * result is unique), and prob[r, t] = exp(x[r, idx[r, t]] - m_r) / l_r with
- * the row's (m_r, l_r) as in osm_softmax_rows.  Computed in one pass: every
- * thread keeps the online normaliser (m, l) and a sorted list of its k best
- * (value, column) pairs; both merge exactly in any grouping ([P3] "Merging
- * partial results"), warp by warp, then across a thread-block cluster.
+ * the row's (m_r, l_r) as in osm_softmax_rows.  A thread-block cluster takes
+ * a row: a first sweep over each block's slice forms the online normaliser
+ * (m, l) and a threshold that at least k entries reach; a second sweep (the
+ * slice is still in L2) keeps, per warp, a running sorted list of the best
+ * (value, column) pairs above that threshold.  Normalisers and lists merge
+ * exactly in any grouping ([P3] "Merging partial results"), warp by warp,
+ * then across the cluster.
  *
  *   x     [rows, cols] fp32, device, read only; entries finite or -inf.
  *   idx   [rows, k] int32 (written);  prob [rows, k] fp32 (written).
  *   rows >= 0 (0 is a no-op), 1 <= k <= cols; k <= 32 (larger k returns
- *   OSM_ERR_UNSUPPORTED: each thread's list lives in registers); cols <= 2^31 - 1;
+ *   OSM_ERR_UNSUPPORTED: a warp's list holds 32 pairs, one per lane); cols <= 2^31 - 1;
  *   rows <= 2^28.
  * An all -inf row gives idx = 0..k-1 and prob = 0.  x, idx, prob 4-byte
  * aligned; 16-byte aligned x with cols % 4 == 0 takes the vector-load path.
