@@ -21,12 +21,13 @@
 //   warp 1     MMA issuer (one thread): S_t = Q_t K_j^T into TMEM, then
 //              O~_t += P_t V_j with P_t read straight from TMEM.
 //   warps 4-7  softmax for query tile 0; warps 8-11 for tile 1.  One thread
-//              per query row, a rolled loop over four 32-column chunks (small
-//              code, no register spills): the chunk TMEM -> registers, mask,
-//              scale and subtract the reference in packed f32x2, 32
-//              independent exp2 (so the MUFU latency is covered), row sum,
-//              bf16 pack, store P over the S columns already consumed;
-//              epilogue O = O~ / l, lse.
+//              per query row, a rolled loop over the tile's columns in chunks
+//              (32 wide at d = 128, 64 wide at d = 64 and with a caller's
+//              bound: measured best for each; no register spills): the chunk
+//              TMEM -> registers, mask, scale and subtract the reference in
+//              packed f32x2, independent exp2 (so the MUFU latency is
+//              covered), row sum, bf16 pack, store P over the S columns
+//              already consumed; epilogue O = O~ / l, lse.
 //   TMEM       512 columns: S_0 | S_1 | O~_0 | O~_1 (128 fp32 columns each).
 // The reference subtracted before exp2 need not be the running maximum: every
 // identity of the recurrence holds for any common reference ("Precision, and
@@ -100,6 +101,7 @@ constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);  // Q, K both K-ma
 
 // error-word sites (kernel id 1 in the top byte)
 constexpr unsigned kSite = 0x01000000u;
+
 
 struct Params {
   int B, H, Nq, Nk;
@@ -463,36 +465,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         float nref = (m_ref == kNegInf) ? 0.f : -m_ref;
-        // pass over four 32-column chunks (S read from TMEM), each chunk
-        // two-phase: all scale/subtracts, then 32 independent exp2, then the
+        // pass over kNch chunks of kCw columns (S read from TMEM), each chunk
+        // two-phase: all scale/subtracts, then kCw independent exp2, then the
         // sums and bf16 packs -- so the MUFU latency is covered
+        constexpr int kCw = (D == 64 || kBounded) ? 64 : 32;
+        constexpr int kNch = kKeys / kCw;
         float la[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t sc[32], pk[16];
+        for (int ch = 0; ch < kNch; ++ch) {
+          uint32_t v[kCw], pk[kCw / 2];
           float cs[4];
-          tmem_ld_x32(tS + 32 * ch, sc);
-          if (masked_tile) {
+          auto load_chunk = [&]() {
+            tmem_ld_cols(tS + kCw * ch, v);
+            if (masked_tile) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (k0 + 32 * ch + e >= limit) sc[e] = __float_as_uint(kNegInf);
-          }
+              for (int e = 0; e < kCw; ++e)
+                if (k0 + kCw * ch + e >= limit) v[e] = __float_as_uint(kNegInf);
+            }
+          };
           auto exp_chunk = [&]() {
-            float pv[32];
+            float pv[kCw];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              fma2(pv[2 * i], pv[2 * i + 1], __uint_as_float(sc[2 * i]),
-                   __uint_as_float(sc[2 * i + 1]), sl2, sl2, nref, nref);
+            for (int i = 0; i < kCw / 2; ++i)
+              fma2(pv[2 * i], pv[2 * i + 1], __uint_as_float(v[2 * i]),
+                   __uint_as_float(v[2 * i + 1]), sl2, sl2, nref, nref);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) pv[e] = ex2(pv[e]);
+            for (int e = 0; e < kCw; ++e) pv[e] = ex2(pv[e]);
             cs[0] = cs[1] = cs[2] = cs[3] = 0.f;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < kCw / 2; ++i) {
               add2(cs[2 * (i & 1)], cs[2 * (i & 1) + 1], pv[2 * i], pv[2 * i + 1]);
               __nv_bfloat162 h2 = __floats2bfloat162_rn(pv[2 * i], pv[2 * i + 1]);
               pk[i] = *reinterpret_cast<uint32_t*>(&h2);
             }
           };
+          load_chunk();
           exp_chunk();
           if (!first) {
             bool over = !((cs[0] + cs[1]) + (cs[2] + cs[3]) <= kSumLimit);
@@ -505,11 +512,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               // everything already formed against the old reference (l, the
               // stored P chunks, O~) by 2^-k, which is exact.  Lowering (only
               // with a caller's bound) happens while nothing has accumulated.
+              // The chunk's scores are still in TMEM (P of earlier chunks lies
+              // in lower columns): read them again.
+              load_chunk();
               float kr = 0.f;
               if (over) {
                 float mc = kNegInf;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) mc = fmaxf(mc, __uint_as_float(sc[e]));
+                for (int e = 0; e < kCw; ++e) mc = fmaxf(mc, __uint_as_float(v[e]));
                 if constexpr (kBounded) {
                   if (mc != kNegInf) kr = ceilf(fmaf(mc, sl2, nref));
                 } else {
@@ -525,17 +535,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int i = 0; i < 4; ++i) la[i] *= alpha;
               tmem_wait_st();
-              for (int c2 = 0; c2 < ch; ++c2) {
-                uint32_t pp[16];
-                tmem_ld_x16(tS + 16 * c2, pp);
+#pragma unroll 1
+              for (int c2 = 0; c2 < ch; ++c2) {  // P of the earlier chunks
+                uint32_t pp[kCw / 2];
+                tmem_ld_cols(tS + (kCw / 2) * c2, pp);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
+                for (int e = 0; e < kCw / 2; ++e) {
                   const float f0 = __uint_as_float(pp[e] << 16) * alpha;
                   const float f1 = __uint_as_float(pp[e] & 0xffff0000u) * alpha;
                   __nv_bfloat162 h2 = __floats2bfloat162_rn(f0, f1);
                   pp[e] = *reinterpret_cast<uint32_t*>(&h2);
                 }
-                tmem_st_x16_nowait(tS + 16 * c2, pp);
+                tmem_st_cols_nowait(tS + (kCw / 2) * c2, pp);
+                tmem_wait_st();
               }
               // O~'s last update (P V of the previous tile) completed before S
               // (before a row's first P V it holds no value: scaling it is harmless)
@@ -552,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int i = 0; i < 4; ++i) la[i] += cs[i];
-          tmem_st_x16_nowait(tS + 16 * ch, pk);
+          tmem_st_cols_nowait(tS + (kCw / 2) * ch, pk);
         }
         tmem_wait_st();
         tc_fence_before();
