@@ -18,11 +18,11 @@
 // in flight per thread, twice: the first pass forms (m, l) and each thread's
 // maximum, whose k-th largest within the warp (within the CTA for k > 16) is
 // a threshold every top-k entry reaches; the second pass (served mostly from
-// L2, the slice was just read) merges only entries that beat the warp's filter
-// into the warp's running list of 32 pairs, one per lane, by bitonic sort and
-// merge, and tightens the filter to the list's k-th entry.  The CTA's lists
+// L2, the slice was just read) inserts only entries that beat the warp's
+// filter into the warp's running list of 32 pairs, one per lane, and tightens
+// the filter to the list's k-th entry.  The CTA's lists
 // meet in warp 0 through shared memory and the cluster's in CTA 0 through
-// distributed shared memory, again by bitonic merges.  K = 1 needs one pass
+// distributed shared memory, by bitonic merges.  K = 1 needs one pass
 // (each thread's arg-max).  HBM-bound: 4 bytes read per element once from
 // HBM, 8 bytes written per output entry.
 #include <cuda_runtime.h>
@@ -424,19 +424,40 @@ __global__ void __launch_bounds__(kThreads) softmax_topk_kernel(const float* __r
   // ---- pass 2: entries that beat the filter enter the warp's running best 32
   // (lane-sorted).  The filter starts at (thr, any index) and tightens to the
   // list's K-th entry in the (value, index) order, so later ties and weaker
-  // values drop out.  Each round every lane offers one candidate; the batch is
-  // sorted and merged into the list.
+  // values drop out.  Each round every lane offers one candidate.
   {
     float kv = thr;
     int ki = kNoIndex;
+    // The lanes' candidates enter the list one at a time: each is broadcast,
+    // its place is the first lane whose entry it comes before, and the lanes
+    // from there on shift up by one (the last entry drops out).  Candidates
+    // are few after the threshold, so this beats sorting each batch.
     auto round = [&](float cv, int ci) {
-      warp_sort_pairs(cv, ci);
-      warp_merge_pairs(v0, i0, cv, ci);
-      const float nv = __shfl_sync(0xffffffffu, v0, K - 1);
-      const int ni = __shfl_sync(0xffffffffu, i0, K - 1);
-      if (ni != kNoIndex && before(nv, ni, kv, ki)) {
-        kv = nv;
-        ki = ni;
+      unsigned cl = __ballot_sync(0xffffffffu, ci != kNoIndex);
+      while (cl) {
+        const int src = __ffs(cl) - 1;
+        cl &= cl - 1;
+        const float v = __shfl_sync(0xffffffffu, cv, src);
+        const int j = __shfl_sync(0xffffffffu, ci, src);
+        if (!before(v, j, kv, ki)) continue;  // the filter has tightened past it
+        const unsigned at = __ballot_sync(0xffffffffu, before(v, j, v0, i0));
+        if (at == 0) continue;  // (not reached: v comes before the K-th entry)
+        const int pos = __ffs(at) - 1;
+        const float uv = __shfl_up_sync(0xffffffffu, v0, 1);
+        const int ui = __shfl_up_sync(0xffffffffu, i0, 1);
+        if (lane == pos) {
+          v0 = v;
+          i0 = j;
+        } else if (lane > pos) {
+          v0 = uv;
+          i0 = ui;
+        }
+        const float nv = __shfl_sync(0xffffffffu, v0, K - 1);
+        const int ni = __shfl_sync(0xffffffffu, i0, K - 1);
+        if (ni != kNoIndex && before(nv, ni, kv, ki)) {
+          kv = nv;
+          ki = ni;
+        }
       }
     };
     v0 = kNegInf;
