@@ -374,7 +374,7 @@ def profile_case(spec: str, iters: int):
     """Run one operation `iters` times on a given shape (for ncu captures).
 
     spec: "attn:B,H,N[,causal][,d64]" | "attnqk:B,H,N[,causal]" (QK-norm inputs with
-          their score bound) | "bwd:B,H,N[,causal]" | "softmax:rows,cols"
+          their score bound) | "bwd:B,H,N[,causal][,d64]" | "softmax:rows,cols"
           | "topk:rows,cols,k"
           | "decode:B,H,Nk[,splits]"
           | "append:B,H,Nk,n_new[,splits]".
@@ -412,16 +412,17 @@ def profile_case(spec: str, iters: int):
     elif op == "bwd":
         # attention backward; O and lse from the forward kernel on the same inputs
         B, H, N = (int(x) for x in parts[:3])
-        causal = len(parts) > 3 and parts[3] == "causal"
-        c = W.attention(4, B, H, N, N, 128, causal, (N // 2, N) if causal else None)
+        causal = "causal" in parts[3:]
+        hd = 64 if "d64" in parts[3:] else 128
+        c = W.attention(4, B, H, N, N, hd, causal, (N // 2, N) if causal else None)
         q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
         kl = c.key_len.to(dev) if c.key_len is not None else None
         o, lse = osm.attn_fwd(q, k, v, c.scale, causal, kl)
-        do = W.to_bf16(W.normal_bhnd(4, 7, B, H, N, 128)).to(dev)
+        do = W.to_bf16(W.normal_bhnd(4, 7, B, H, N, hd)).to(dev)
         ws = torch.empty(max(256, B * H * N * 4), dtype=torch.uint8, device=dev)
         run = lambda: osm.attn_bwd(q, k, v, o, lse, do, c.scale, causal, kl, workspace=ws)
         # 5 products of 2 d FLOPs per visible (query, key) pair = 2.5 x the forward's
-        work = 2.5 * attn_flops(B, H, N, N, 128, causal,
+        work = 2.5 * attn_flops(B, H, N, N, hd, causal,
                                 None if kl is None else c.key_len.numpy())
         unit = "TFLOP/s"
     elif op == "softmax":

@@ -31,7 +31,7 @@ def check(x_cpu, k, idx, prob, rows=None):
 SHAPES = [(1, 1), (3, 5), (7, 31), (4, 1000), (2, 4097), (5, 32768), (2, 100003), (3, 262144)]
 
 
-@pytest.mark.parametrize("k", [1, 3, 8, 32])
+@pytest.mark.parametrize("k", [1, 2, 3, 8, 16, 32])
 @pytest.mark.parametrize("shape", SHAPES)
 def test_shapes(cuda_ok, shape, k):
     rows, cols = shape
@@ -55,6 +55,20 @@ def test_ties_masked_entries_and_empty_rows(cuda_ok):
         check(xt, k, idx, prob)
         assert torch.equal(idx[2].cpu(), torch.arange(k, dtype=torch.int32))
         assert torch.all(prob[2] == 0)
+
+
+def test_monotone_rows(cuda_ok):
+    """Rows sorted ascending (every later entry beats the list so far) and
+    descending (the first entries are the answer), on the vector path and
+    split over a cluster."""
+    for cols in (4096, 1 << 19):
+        up = torch.arange(cols, dtype=torch.float32) / cols
+        x = torch.stack([up, up.flip(0), up * 0 + 0.25, up.roll(cols // 3)])
+        for k in (2, 16, 32):
+            idx, prob = osm.softmax_topk(x.cuda(), k)
+            check(x, k, idx, prob)
+            assert torch.equal(idx[0].cpu(), torch.arange(cols - 1, cols - 1 - k, -1, dtype=torch.int32))
+            assert torch.equal(idx[1].cpu(), torch.arange(k, dtype=torch.int32))
 
 
 def test_unaligned_and_odd_widths(cuda_ok):
