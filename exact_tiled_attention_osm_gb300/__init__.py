@@ -7,12 +7,23 @@ every call raises.
 
 Functions mirror the C entry points in include/osm.h:
     softmax_rows(x, out=None)                          -> y
-    attn_fwd(q, k, v, scale=None, causal=False, key_len=None, out=None, lse=None)
-                                                       -> (o, lse)
+    softmax_topk(x, k, idx=None, prob=None)            -> (idx, prob)
+    attn_fwd(q, k, v, scale=None, causal=False, key_len=None, out=None, lse=None,
+             score_bound=None)                         -> (o, lse)
+    attn_bwd(q, k, v, o, lse, dout, scale=None, causal=False, key_len=None,
+             workspace=None)                           -> (dq, dk, dv)
     attn_decode_splitkv(q, k, v, scale=None, key_len=None, num_splits=16,
                         workspace=None, out=None, lse=None) -> (o, lse)
+    attn_decode_splitkv_noalloc(q, k, v, scale=None, key_len=None, num_splits=16,
+                                out=None, lse=None)     -> (o, lse)
     decode_workspace_bytes(B, H, d, num_splits)         -> int
+    decode_partials(workspace, B, H, d, num_splits)     -> (m, l, o~) views
+    decode_state(B, H, d, device)                       -> (m, l, o~), the empty summary
+    decode_append_workspace_bytes(B, H, d, num_splits)  -> int
+    attn_decode_append(q, k, v, state, key_start=None, key_end=None, scale=None,
+                       num_splits=16, workspace=None, out=None, lse=None) -> (o, lse)
     lse_merge(o_parts, lse_parts, out_dtype=torch.float32) -> (o, lse)
+    selftest_bounded_wait(device=None)                  (runs a wait that must give up)
     device_status()                                    -> int (0 = no device wait ran out)
 """
 from __future__ import annotations
