@@ -103,7 +103,9 @@ def _stream(t: torch.Tensor) -> int:
     return torch.cuda.current_stream(t.device).cuda_stream
 
 
-def _need(t: torch.Tensor, name: str, dtype=None, device=None):
+def _need(t: torch.Tensor, name: str, dtype=None, device=None, shape=None):
+    """Check what the C entry points cannot: a contiguous CUDA tensor of the
+    given dtype, device and shape (a short output buffer would be overrun)."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
@@ -114,6 +116,8 @@ def _need(t: torch.Tensor, name: str, dtype=None, device=None):
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     if device is not None and t.device != device:
         raise ValueError(f"{name} must be on {device}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
 def softmax_rows(x: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
@@ -122,7 +126,7 @@ def softmax_rows(x: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.T
     if x.dim() != 2:
         raise ValueError("x must be 2-D [rows, cols]")
     y = torch.empty_like(x) if out is None else out
-    _need(y, "out", torch.float32, x.device)
+    _need(y, "out", torch.float32, x.device, x.shape)
     if y.shape != x.shape:
         raise ValueError("out must have x's shape")
     lib = load_library()
@@ -144,8 +148,8 @@ def softmax_topk(x, k, idx=None, prob=None):
     rows, cols = x.shape
     idx_t = torch.empty((rows, k), dtype=torch.int32, device=x.device) if idx is None else idx
     prob_t = torch.empty((rows, k), dtype=torch.float32, device=x.device) if prob is None else prob
-    _need(idx_t, "idx", torch.int32, x.device)
-    _need(prob_t, "prob", torch.float32, x.device)
+    _need(idx_t, "idx", torch.int32, x.device, (rows, k))
+    _need(prob_t, "prob", torch.float32, x.device, (rows, k))
     lib = load_library()
     with torch.cuda.device(x.device):
         _check(lib.osm_softmax_topk(x.data_ptr(), rows, cols, int(k), idx_t.data_ptr(),
@@ -172,13 +176,11 @@ def attn_fwd(q, k, v, scale=None, causal=False, key_len=None, out=None, lse=None
         scale = 1.0 / math.sqrt(d)
     o = torch.empty_like(q) if out is None else out
     lse_t = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
-    _need(o, "out", torch.bfloat16, q.device)
-    _need(lse_t, "lse", torch.float32, q.device)
+    _need(o, "out", torch.bfloat16, q.device, q.shape)
+    _need(lse_t, "lse", torch.float32, q.device, (B, H, Nq))
     kl = 0
     if key_len is not None:
-        _need(key_len, "key_len", torch.int32, q.device)
-        if key_len.numel() != B:
-            raise ValueError("key_len must have B entries")
+        _need(key_len, "key_len", torch.int32, q.device, (B,))
         kl = key_len.data_ptr()
     lib = load_library()
     with torch.cuda.device(q.device):
@@ -216,7 +218,7 @@ def attn_bwd(q, k, v, o, lse, dout, scale=None, causal=False, key_len=None, work
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     kl = 0
     if key_len is not None:
-        _need(key_len, "key_len", torch.int32, q.device)
+        _need(key_len, "key_len", torch.int32, q.device, (B,))
         kl = key_len.data_ptr()
     with torch.cuda.device(q.device):
         _check(lib.osm_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
@@ -256,9 +258,11 @@ def attn_decode_splitkv(q, k, v, scale=None, key_len=None, num_splits=16, worksp
     _need(workspace, "workspace", torch.uint8, q.device)
     o = torch.empty_like(q) if out is None else out
     lse_t = torch.empty((B, H), dtype=torch.float32, device=q.device) if lse is None else lse
+    _need(o, "out", q.dtype, q.device, q.shape)
+    _need(lse_t, "lse", torch.float32, q.device, (B, H))
     kl = 0
     if key_len is not None:
-        _need(key_len, "key_len", torch.int32, q.device)
+        _need(key_len, "key_len", torch.int32, q.device, (B,))
         kl = key_len.data_ptr()
     lib = load_library()
     with torch.cuda.device(q.device):
@@ -312,12 +316,14 @@ def attn_decode_append(q, k, v, state, key_start=None, key_end=None, scale=None,
     _need(workspace, "workspace", torch.uint8, q.device)
     o = torch.empty_like(q) if out is None else out
     lse_t = torch.empty((B, H), dtype=torch.float32, device=q.device) if lse is None else lse
+    _need(o, "out", q.dtype, q.device, q.shape)
+    _need(lse_t, "lse", torch.float32, q.device, (B, H))
     ptrs = []
     for t, n in ((key_start, "key_start"), (key_end, "key_end")):
         if t is None:
             ptrs.append(0)
         else:
-            _need(t, n, torch.int32, q.device)
+            _need(t, n, torch.int32, q.device, (B,))
             ptrs.append(t.data_ptr())
     lib = load_library()
     with torch.cuda.device(q.device):
@@ -357,9 +363,11 @@ def attn_decode_splitkv_noalloc(q, k, v, scale=None, key_len=None, num_splits=16
         scale = 1.0 / math.sqrt(d)
     o = torch.empty_like(q) if out is None else out
     lse_t = torch.empty((B, H), dtype=torch.float32, device=q.device) if lse is None else lse
+    _need(o, "out", q.dtype, q.device, q.shape)
+    _need(lse_t, "lse", torch.float32, q.device, (B, H))
     kl = 0
     if key_len is not None:
-        _need(key_len, "key_len", torch.int32, q.device)
+        _need(key_len, "key_len", torch.int32, q.device, (B,))
         kl = key_len.data_ptr()
     lib = load_library()
     with torch.cuda.device(q.device):
