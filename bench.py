@@ -419,7 +419,7 @@ def profile_case(spec: str, iters: int):
         kl = c.key_len.to(dev) if c.key_len is not None else None
         o, lse = osm.attn_fwd(q, k, v, c.scale, causal, kl)
         do = W.to_bf16(W.normal_bhnd(4, 7, B, H, N, hd)).to(dev)
-        ws = torch.empty(max(256, B * H * N * 4), dtype=torch.uint8, device=dev)
+        ws = torch.empty(osm.attn_bwd_workspace_bytes(B, H, N), dtype=torch.uint8, device=dev)
         run = lambda: osm.attn_bwd(q, k, v, o, lse, do, c.scale, causal, kl, workspace=ws)
         # 5 products of 2 d FLOPs per visible (query, key) pair = 2.5 x the forward's
         work = 2.5 * attn_flops(B, H, N, N, hd, causal,

@@ -12,6 +12,7 @@ Functions mirror the C entry points in include/osm.h:
              score_bound=None)                         -> (o, lse)
     attn_bwd(q, k, v, o, lse, dout, scale=None, causal=False, key_len=None,
              workspace=None)                           -> (dq, dk, dv)
+    attn_bwd_workspace_bytes(B, H, Nq)                  -> int
     attn_decode_splitkv(q, k, v, scale=None, key_len=None, num_splits=16,
                         workspace=None, out=None, lse=None) -> (o, lse)
     attn_decode_splitkv_noalloc(q, k, v, scale=None, key_len=None, num_splits=16,
@@ -195,6 +196,10 @@ def attn_fwd(q, k, v, scale=None, causal=False, key_len=None, out=None, lse=None
                                             float(score_bound), _stream(q)),
                    "osm_attn_fwd_bounded")
     return o, lse_t
+
+
+def attn_bwd_workspace_bytes(B: int, H: int, Nq: int) -> int:
+    return int(load_library().osm_attn_bwd_workspace_bytes(B, H, Nq))
 
 
 def attn_bwd(q, k, v, o, lse, dout, scale=None, causal=False, key_len=None, workspace=None):

@@ -55,3 +55,47 @@ def test_capture_and_replay(cuda_ok):
     rdo, rdl = osm.attn_decode_splitkv(dq, dk, dv, d1.scale, dkl, 8)
     assert torch.equal(do, rdo) and torch.equal(dlse, rdl)
     assert torch.equal(y, osm.softmax_rows(x))
+
+
+def test_capture_and_replay_next_rows(cuda_ok):
+    """The backward, the known-bound forward and the fused top-k under capture."""
+    dev = torch.device("cuda")
+    a = W.attention(84, 1, 3, 700, 700, 128, True, (300, 700))
+    q, k, v = (t.to(dev) for t in (a.q, a.k, a.v))
+    kl = a.key_len.to(dev)
+    o, lse = osm.attn_fwd(q, k, v, a.scale, True, kl)
+    dout = W.to_bf16(W.normal_bhnd(84, 7, 1, 3, 700, 128)).to(dev)
+    ws = torch.empty(osm.attn_bwd_workspace_bytes(1, 3, 700), dtype=torch.uint8, device=dev)
+    x = W.softmax_logits(seed=85, rows=32, cols=20000).to(dev)
+    bound = float(a.scale) * float(q.float().norm(dim=-1).max()) * float(k.float().norm(dim=-1).max())
+    ob = torch.empty_like(q)
+    lb = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    idx = torch.empty((32, 8), dtype=torch.int32, device=dev)
+    prob = torch.empty((32, 8), dtype=torch.float32, device=dev)
+    outs = {}
+
+    def body():
+        outs["bwd"] = osm.attn_bwd(q, k, v, o, lse, dout, a.scale, True, kl, workspace=ws)
+        osm.attn_fwd(q, k, v, a.scale, True, kl, out=ob, lse=lb, score_bound=bound)
+        osm.softmax_topk(x, 8, idx=idx, prob=prob)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        body()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        body()
+    idx.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert osm.device_status() == 0
+    rq, rk, rv = osm.attn_bwd(q, k, v, o, lse, dout, a.scale, True, kl)
+    gq, gk, gv = outs["bwd"]
+    assert torch.equal(gq, rq) and torch.equal(gk, rk) and torch.equal(gv, rv)
+    rob, rlb = osm.attn_fwd(q, k, v, a.scale, True, kl, score_bound=bound)
+    assert torch.equal(ob, rob) and torch.equal(lb, rlb)
+    ri, rp = osm.softmax_topk(x, 8)
+    assert torch.equal(idx, ri) and torch.equal(prob, rp)
