@@ -377,7 +377,7 @@ def profile_case(spec: str, iters: int):
           their score bound) | "bwd:B,H,N[,causal][,d64]" | "softmax:rows,cols"
           | "topk:rows,cols,k"
           | "decode:B,H,Nk[,splits]"
-          | "append:B,H,Nk,n_new[,splits]".
+          | "append:B,H,Nk,n_new[,splits]" | "lsemerge:S,rows,d".
     Inputs come from the same generators as the full workloads.
     """
     import exact_tiled_attention_osm_gb300 as osm
@@ -462,6 +462,14 @@ def profile_case(spec: str, iters: int):
         work = (B * H * n_new * 128 * 2 * 2 + B * H * 128 * 2 * 2 + B * H * 4
                 + 2 * B * H * (128 + 2) * 4)
         unit = "GB/s"
+    elif op == "lsemerge":
+        # LSE-form merge of S normalised partials of rows x d (fp32 in, bf16 out)
+        S, R, d = (int(x) for x in parts[:3])
+        g = torch.Generator(device="cpu").manual_seed(6)
+        op_ = torch.randn((S, R, d), generator=g).to(dev)
+        lp = (torch.randn((S, R), generator=g) * 3).to(dev)
+        run = lambda: osm.lse_merge(op_, lp, torch.bfloat16)
+        work, unit = S * R * (d + 1) * 4 + R * (d * 2 + 4), "GB/s"
     else:
         raise SystemExit(f"unknown op {op}")
     run()
