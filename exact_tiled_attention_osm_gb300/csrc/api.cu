@@ -61,6 +61,10 @@ osm_status osm_softmax_topk(const float* x, int64_t rows, int64_t cols, int k, i
 }
 
 namespace {
+// longest sequence (Nq, Nk) accepted: keeps every tile and split count, and
+// every length rounded up to a tile, inside int arithmetic
+constexpr int kMaxSeq = 1 << 30;
+
 osm_status attn_fwd_checked(const void* q, const void* k, const void* v, void* o, float* lse,
                             int B, int H, int Nq, int Nk, int d, float scale, int causal,
                             const int32_t* key_len, float score_bound, osm_stream_t stream) {
@@ -68,6 +72,7 @@ osm_status attn_fwd_checked(const void* q, const void* k, const void* v, void* o
   if (causal != 0 && causal != 1) return OSM_ERR_INVALID_VALUE;
   if (!(scale > 0.f) || !std::isfinite(scale)) return OSM_ERR_INVALID_VALUE;
   if (d != 64 && d != 128) return (d > 0) ? OSM_ERR_UNSUPPORTED : OSM_ERR_INVALID_VALUE;
+  if (Nq > kMaxSeq || Nk > kMaxSeq) return OSM_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(B) * H * Nq == 0) return OSM_OK;
   if (!q || !o || !lse || (Nk > 0 && (!k || !v))) return OSM_ERR_INVALID_VALUE;
   if (!aligned16(q) || !aligned16(o) || !aligned4(lse)) return OSM_ERR_INVALID_VALUE;
@@ -112,6 +117,7 @@ osm_status osm_attn_bwd(const void* q, const void* k, const void* v, const void*
   if (causal != 0 && causal != 1) return OSM_ERR_INVALID_VALUE;
   if (!(scale > 0.f) || !std::isfinite(scale)) return OSM_ERR_INVALID_VALUE;
   if (d != 64 && d != 128) return (d > 0) ? OSM_ERR_UNSUPPORTED : OSM_ERR_INVALID_VALUE;
+  if (Nq > kMaxSeq || Nk > kMaxSeq) return OSM_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(B) * H == 0 || (Nq == 0 && Nk == 0)) return OSM_OK;
   if (Nq > 0 && (!q || !o || !lse || !dout || !dq)) return OSM_ERR_INVALID_VALUE;
   if (Nk > 0 && (!k || !v || !dk || !dv)) return OSM_ERR_INVALID_VALUE;
@@ -150,7 +156,7 @@ osm_status osm_attn_decode_splitkv(osm_dtype dt, const void* q, const void* k, c
   if (num_splits < 1 || num_splits > 256) return OSM_ERR_INVALID_VALUE;
   if (!(scale > 0.f) || !std::isfinite(scale)) return OSM_ERR_INVALID_VALUE;
   if (static_cast<int64_t>(B) * H == 0) return OSM_OK;
-  if (B > 65535 || H > 65535) return OSM_ERR_UNSUPPORTED;
+  if (B > 65535 || H > 65535 || Nk > kMaxSeq) return OSM_ERR_UNSUPPORTED;
   if (!q || !o || !lse || !workspace || (Nk > 0 && (!k || !v))) return OSM_ERR_INVALID_VALUE;
   if (!aligned16(q) || !aligned16(o) || !aligned4(lse)) return OSM_ERR_INVALID_VALUE;
   if (Nk > 0 && (!aligned16(k) || !aligned16(v))) return OSM_ERR_INVALID_VALUE;
@@ -173,7 +179,7 @@ osm_status osm_attn_decode_splitkv_noalloc(osm_dtype dt, const void* q, const vo
   if (num_splits < 1 || num_splits > 256) return OSM_ERR_INVALID_VALUE;
   if (!(scale > 0.f) || !std::isfinite(scale)) return OSM_ERR_INVALID_VALUE;
   if (static_cast<int64_t>(B) * H == 0) return OSM_OK;
-  if (B > 65535 || H > 65535) return OSM_ERR_UNSUPPORTED;
+  if (B > 65535 || H > 65535 || Nk > kMaxSeq) return OSM_ERR_UNSUPPORTED;
   // the summaries must fit the library's fixed scratch area
   if (osm::decode_workspace_bytes(B, H, d, num_splits) > OSM_NOALLOC_SCRATCH_BYTES)
     return OSM_ERR_INVALID_VALUE;
@@ -203,7 +209,7 @@ osm_status osm_attn_decode_append(osm_dtype dt, const void* q, const void* k, co
   if (num_splits < 1 || num_splits > 256) return OSM_ERR_INVALID_VALUE;
   if (!(scale > 0.f) || !std::isfinite(scale)) return OSM_ERR_INVALID_VALUE;
   if (static_cast<int64_t>(B) * H == 0) return OSM_OK;
-  if (B > 65535 || H > 65535) return OSM_ERR_UNSUPPORTED;
+  if (B > 65535 || H > 65535 || Nk > kMaxSeq) return OSM_ERR_UNSUPPORTED;
   if (!q || !state_m || !state_l || !state_o || !workspace || (Nk > 0 && (!k || !v)))
     return OSM_ERR_INVALID_VALUE;
   if (!aligned16(q) || !aligned4(state_m) || !aligned4(state_l) || !aligned4(state_o))

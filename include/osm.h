@@ -16,7 +16,8 @@
  *  - Tensors are dense and contiguous, row-major, innermost dimension last.
  *  - Arguments are validated on the host before anything is launched; a bad
  *    argument returns OSM_ERR_INVALID_VALUE (or OSM_ERR_UNSUPPORTED for a valid
- *    but unimplemented case) and launches nothing.  A failed launch returns
+ *    but unimplemented case) and launches nothing.  Sequence lengths (Nq, Nk)
+ *    above 2^30 are unsupported.  A failed launch returns
  *    OSM_ERR_CUDA.  No call aborts the process or throws.
  *  - Scores are s = scale * (q . k).  Log-sum-exp outputs are natural-log
  *    values of the scaled scores.  Kernels work in base 2 internally (log2(e)

@@ -109,6 +109,8 @@ def test_attn_validation(lib):
     assert call(B=-1) == osm.OSM_ERR_INVALID_VALUE
     assert call(d=96) == osm.OSM_ERR_UNSUPPORTED
     assert call(d=0) == osm.OSM_ERR_INVALID_VALUE
+    assert call(Nq=(1 << 30) + 1) == osm.OSM_ERR_UNSUPPORTED   # longer than 2^30
+    assert call(Nk=(1 << 30) + 1) == osm.OSM_ERR_UNSUPPORTED
     assert call(scale=0.0) == osm.OSM_ERR_INVALID_VALUE
     assert call(scale=-1.0) == osm.OSM_ERR_INVALID_VALUE
     assert call(scale=float("inf")) == osm.OSM_ERR_INVALID_VALUE
@@ -156,6 +158,8 @@ def test_bwd_validation(lib):
     assert call(lse=FAKE + 2) == osm.OSM_ERR_INVALID_VALUE
     assert call(dq=FAKE + 8) == osm.OSM_ERR_INVALID_VALUE
     assert call(d=96) == osm.OSM_ERR_UNSUPPORTED
+    assert call(Nq=(1 << 30) + 1) == osm.OSM_ERR_UNSUPPORTED
+    assert call(Nk=(1 << 30) + 1) == osm.OSM_ERR_UNSUPPORTED
     assert call(scale=0.0) == osm.OSM_ERR_INVALID_VALUE
     assert call(causal=3) == osm.OSM_ERR_INVALID_VALUE
     assert call(ws=None) == osm.OSM_ERR_INVALID_VALUE
@@ -178,6 +182,7 @@ def test_decode_and_merge_validation(lib):
     assert call(0, 7) == osm.OSM_ERR_INVALID_VALUE           # dtype
     assert call(1, None) == osm.OSM_ERR_INVALID_VALUE        # q
     assert call(9, 96) == osm.OSM_ERR_UNSUPPORTED            # d
+    assert call(8, (1 << 30) + 1) == osm.OSM_ERR_UNSUPPORTED  # Nk longer than 2^30
     assert call(12, 0) == osm.OSM_ERR_INVALID_VALUE          # num_splits
     assert call(12, 300) == osm.OSM_ERR_INVALID_VALUE
     assert call(13, None) == osm.OSM_ERR_INVALID_VALUE       # workspace
@@ -217,6 +222,7 @@ def test_append_validation(lib):
     assert call(m=FAKE + 2) == osm.OSM_ERR_INVALID_VALUE   # misaligned state
     assert call(ks=FAKE + 1) == osm.OSM_ERR_INVALID_VALUE
     assert call(d=96) == osm.OSM_ERR_UNSUPPORTED
+    assert call(Nk=(1 << 30) + 1) == osm.OSM_ERR_UNSUPPORTED
     assert call(S=0) == osm.OSM_ERR_INVALID_VALUE
     assert call(ws=FAKE + 16) == osm.OSM_ERR_INVALID_VALUE
     assert call(wsb=need - 1) == osm.OSM_ERR_INVALID_VALUE
