@@ -230,6 +230,22 @@ def test_long_sequence_causal_padded(cuda_ok):
     check(o[:, :, rows], lse[:, :, rows], ro, rl)
 
 
+def test_very_long_sequence(cuda_ok):
+    """131072 queries and keys in one head (1024 key tiles per row at the end),
+    causal, and the same head against 131072 keys without a mask for 256
+    queries: sampled rows at the start, at tile edges and at the end."""
+    N = 131072
+    case = W.attention(92, 1, 1, N, N, 128, True, None)
+    o, lse = run(case)
+    rows = np.array([0, 1, 255, 256, 65535, 65536, N - 129, N - 128, N - 1])
+    ro, rl = oracle_of(case, rows=rows)
+    check(o[:, :, rows], lse[:, :, rows], ro, rl)
+    cross = W.attention(93, 1, 1, 256, N, 128, False, None)
+    o, lse = run(cross)
+    ro, rl = oracle_of(cross)
+    check(o, lse, ro, rl)
+
+
 def test_cross_attention_shapes(cuda_ok):
     """Nq != Nk without a causal mask (cross-attention): 512 queries against
     16384 keys, and 3000 queries against 200 keys."""
