@@ -16,10 +16,14 @@
 //   work item  = (b, h, pair of 128-row query tiles); both tiles share every
 //                streamed K/V tile, and alternate on the tensor core so one
 //                tile's softmax overlaps the other tile's matrix products.
-//   warp 0     TMA producer: Q tiles once per item, K_j / V_j through a ring
-//              of shared-memory slots (128-byte swizzle).
-//   warp 1     MMA issuer (one thread): S_t = Q_t K_j^T into TMEM, then
-//              O~_t += P_t V_j with P_t read straight from TMEM.
+//   warp 0     TMA producer: Q tiles once per item, then K_j together with
+//              V_{j-1} (the two tiles step j reads) into one of two pairs of
+//              shared-memory slots (128-byte swizzle) under one mbarrier, so
+//              each key step costs the MMA thread one wait and one release.
+//   warp 1     MMA issuer (one thread): per key step j and query tile t,
+//              O~_t += P_t V_{j-1} (P_t read straight from TMEM), then
+//              S_t = Q_t K_j^T into TMEM over the columns P_t occupied (the
+//              tensor pipe runs them in issue order).
 //   warps 4-7  softmax for query tile 0; warps 8-11 for tile 1.  One thread
 //              per query row, a rolled loop over the tile's columns in chunks
 //              (32 wide at d = 128, 64 wide at d = 64 and with a caller's
@@ -56,6 +60,7 @@ using namespace ptx;
 constexpr int kRows = 128;   // query rows per tile (MMA M)
 constexpr int kKeys = 128;   // keys per K/V tile (MMA N of QK^T, K of PV)
 constexpr int kSlots = 4;    // K/V ring slots, one 32 KB tile each
+constexpr int kPairs = kSlots / 2;  // the ring as (K_j, V_{j-1}) pairs under one barrier
 constexpr int kItemSlots = 4;  // depth of the CTA's queue of work-item numbers
 constexpr uint32_t kTileBytes = kRows * 128 * 2;  // 32768: a tile slot holds d = 128
 constexpr uint32_t kBoxBytes = 128 * 64 * 2;           // one TMA box: 64 columns x 128 rows
@@ -262,20 +267,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++loaded;
           // the counter's reply is first needed after this item's first K/V copies
           ticket = atomicAdd(p.next_item, 1u);
-          for (int j = 0; ok && j < it.n_kv; ++j) {
-            for (int kv = 0; kv < 2; ++kv) {
-              if (!(ok = wait_one(bar(KV_EMPTY + slot), ph ^ 1, kSite | 2))) break;
-              mbar_arrive_expect_tx(bar(KV_FULL + slot), kKeys * D * 2);
-              const CUtensorMap* tm = kv ? &tm_v : &tm_k;
+          // pair e of the item: K_e (e < n) and V_{e-1} (e > 0), one barrier
+          for (int e = 0; ok && e <= it.n_kv; ++e) {
+            if (!(ok = wait_one(bar(KV_EMPTY + slot), ph ^ 1, kSite | 2))) break;
+            const uint32_t bytes =
+                (e < it.n_kv ? kKeys * D * 2u : 0u) + (e > 0 ? kKeys * D * 2u : 0u);
+            mbar_arrive_expect_tx(bar(KV_FULL + slot), bytes);
+            if (e < it.n_kv)
               for (int c = 0; c < D / 64; ++c)
-                tma_load_3d(sKV + slot * kTileBytes + c * kBoxBytes, tm, bar(KV_FULL + slot),
-                            c * 64, j * kKeys, it.bh);
-              fill_mask |= 1u << slot;
-              fill_ph = (fill_ph & ~(1u << slot)) | (ph << slot);
-              if (++slot == kSlots) {
-                slot = 0;
-                ph ^= 1;
-              }
+                tma_load_3d(sKV + (2 * slot) * kTileBytes + c * kBoxBytes, &tm_k,
+                            bar(KV_FULL + slot), c * 64, e * kKeys, it.bh);
+            if (e > 0)
+              for (int c = 0; c < D / 64; ++c)
+                tma_load_3d(sKV + (2 * slot + 1) * kTileBytes + c * kBoxBytes, &tm_v,
+                            bar(KV_FULL + slot), c * 64, (e - 1) * kKeys, it.bh);
+            fill_mask |= 1u << slot;
+            fill_ph = (fill_ph & ~(1u << slot)) | (ph << slot);
+            if (++slot == kPairs) {
+              slot = 0;
+              ph ^= 1;
             }
             if (ok && !published) ok = publish_next();
           }
@@ -285,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && !published) ok = publish_next();
       }
       if (!ok) {  // let every copy this thread started land before the CTA exits
-        for (int s = 0; s < kSlots; ++s)
+        for (int s = 0; s < kPairs; ++s)
           if (fill_mask >> s & 1u) wait_drain(bar(KV_FULL + s), fill_ph >> s & 1u, 200000000ull);
         if (q_fill >= 0)
           for (int t = 0; t < 2; ++t) wait_drain(bar(Q_FULL + t), q_fill, 200000000ull);
@@ -311,10 +321,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         qf_ph ^= 1;
         tc_fence_after();
         bool first_pv[2] = {true, true};
-        uint32_t v_slot = 0, v_ph = 0;
+        uint32_t v_buf = 0;  // shared-memory address of the V tile of the current pair
         // O~_t += P_t V_{j-1} once the softmax of tile t has stored P_t
         auto issue_pv = [&](int t) -> bool {
-          const uint64_t vdesc = dV + ((sKV + v_slot * kTileBytes) >> 4);
+          const uint64_t vdesc = dV + (v_buf >> 4);
           if (!wait_one(bar(P_FULL + t), pf_ph[t], kSite | 5)) return false;
           if (first_pv[t] && done > 0) {
             if (!wait_one(bar(O_EMPTY + t), oe_ph[t], kSite | 6)) return false;
@@ -332,16 +342,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           return true;
         };
         for (int j = 0; ok && j < it.n_kv; ++j) {
-          const uint32_t k_slot = slot;
-          if (!(ok = wait_one(bar(KV_FULL + k_slot), ph, kSite | 4))) break;
-          if (++slot == kSlots) { slot = 0; ph ^= 1; }
-          const uint32_t nv_slot = slot, nv_ph = ph;
-          if (++slot == kSlots) { slot = 0; ph ^= 1; }
-          if (j > 0) {
-            if (!(ok = wait_one(bar(KV_FULL + v_slot), v_ph, kSite | 4))) break;
-          }
+          const uint32_t ps = slot;  // pair j: K_j and (j > 0) V_{j-1}
+          if (!(ok = wait_one(bar(KV_FULL + ps), ph, kSite | 4))) break;
+          if (++slot == kPairs) { slot = 0; ph ^= 1; }
           tc_fence_after();
-          const uint64_t kdesc = dK + ((sKV + k_slot * kTileBytes) >> 4);
+          const uint64_t kdesc = dK + ((sKV + (2 * ps) * kTileBytes) >> 4);
+          v_buf = sKV + (2 * ps + 1) * kTileBytes;
           for (int t = 0; t < 2 && ok; ++t) {
             if (j > 0 && !(ok = issue_pv(t))) break;
             const uint64_t qdesc = dK + ((sQ + t * kTileBytes) >> 4);
@@ -354,20 +360,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(bar(S_FULL + t));
           }
           if (!ok) break;
-          mma_commit(bar(KV_EMPTY + k_slot));
-          if (j > 0) mma_commit(bar(KV_EMPTY + v_slot));
+          mma_commit(bar(KV_EMPTY + ps));  // pair j read: S(j) and P V_{j-1} issued
           if (j == it.n_kv - 1) mma_commit(bar(Q_EMPTY));
-          v_slot = nv_slot;
-          v_ph = nv_ph;
         }
         if (!ok) break;
-        if (!(ok = wait_one(bar(KV_FULL + v_slot), v_ph, kSite | 4))) break;
+        const uint32_t ps = slot;  // the item's last pair: V_{n-1}
+        if (!(ok = wait_one(bar(KV_FULL + ps), ph, kSite | 4))) break;
+        if (++slot == kPairs) { slot = 0; ph ^= 1; }
+        tc_fence_after();
+        v_buf = sKV + (2 * ps + 1) * kTileBytes;
         for (int t = 0; t < 2 && ok; ++t) {
           if (!(ok = issue_pv(t))) break;
           mma_commit(bar(O_FULL + t));
         }
         if (!ok) break;
-        mma_commit(bar(KV_EMPTY + v_slot));
+        mma_commit(bar(KV_EMPTY + ps));
         ++done;
       }
       if (!ok) {  // wait for every MMA already issued before TMEM is released
