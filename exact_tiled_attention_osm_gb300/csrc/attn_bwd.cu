@@ -41,6 +41,7 @@ using namespace ptx;
 
 constexpr int kTile = 128;   // rows of every tile (query or key)
 constexpr int kSlots = 4;    // streamed 32 KB tiles in flight
+constexpr int kPairs = kSlots / 2;  // dK/dV kernel: the slots as (Q_i, dO_i) pairs
 constexpr uint32_t kTileBytes = kTile * 128 * 2;  // 32768: a slot holds a d = 128 tile
 constexpr uint32_t kBoxBytes = 128 * 64 * 2;           // one TMA box: 64 columns x 128 rows
 constexpr int kThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 4-11 element-wise
@@ -491,24 +492,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_3d(sK + c * kBoxBytes, &tm_k, bar(RES_FULL), c * 64, k0, bh);
       tma_load_3d(sV + c * kBoxBytes, &tm_v, bar(RES_FULL), c * 64, k0, bh);
     }
+    // (Q_i, dO_i) as one pair of slots under one barrier: both are read by
+    // query tile i's products and released together after dK_i
     uint32_t slot = 0, ph = 0, fill_mask = 0, fill_ph = 0;
     bool ok = true;
     for (int i = 0; ok && i < n_q; ++i) {
       const int qrow = (qt_first + i) * kTile;
-      for (int t = 0; t < 2; ++t) {  // Q_i then dO_i
-        if (!(ok = wait_one(bar(RING_EMPTY + slot), ph ^ 1, kSiteK | 1))) break;
-        mbar_arrive_expect_tx(bar(RING_FULL + slot), kTile * D * 2);
-        const CUtensorMap* tm = t ? &tm_do : &tm_q;
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sRing + slot * kTileBytes + c * kBoxBytes, tm, bar(RING_FULL + slot), c * 64,
-                      qrow, bh);
-        fill_mask |= 1u << slot;
-        fill_ph = (fill_ph & ~(1u << slot)) | (ph << slot);
-        if (++slot == kSlots) { slot = 0; ph ^= 1; }
+      if (!(ok = wait_one(bar(RING_EMPTY + slot), ph ^ 1, kSiteK | 1))) break;
+      mbar_arrive_expect_tx(bar(RING_FULL + slot), 2 * kTile * D * 2);
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d(sRing + (2 * slot) * kTileBytes + c * kBoxBytes, &tm_q, bar(RING_FULL + slot),
+                    c * 64, qrow, bh);
+        tma_load_3d(sRing + (2 * slot + 1) * kTileBytes + c * kBoxBytes, &tm_do,
+                    bar(RING_FULL + slot), c * 64, qrow, bh);
       }
+      fill_mask |= 1u << slot;
+      fill_ph = (fill_ph & ~(1u << slot)) | (ph << slot);
+      if (++slot == kPairs) { slot = 0; ph ^= 1; }
     }
     if (!ok) {
-      for (int s = 0; s < kSlots; ++s)
+      for (int s = 0; s < kPairs; ++s)
         if (fill_mask >> s & 1u) wait_drain(bar(RING_FULL + s), fill_ph >> s & 1u, 200000000ull);
       wait_drain(bar(RES_FULL), 0, 200000000ull);
     }
@@ -525,10 +528,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       tc_fence_after();
       const uint64_t kdesc = dKm + (sK >> 4), vdesc = dKm + (sV >> 4);
-      auto next_slot = [&](uint32_t& s_out) -> bool {  // ring slots in fill order
-        s_out = slot;
+      // pair p holds Q_i in slot 2p and dO_i in slot 2p + 1
+      auto next_pair = [&](uint32_t& p_out) -> bool {
+        p_out = slot;
         const bool r = wait_one(bar(RING_FULL + slot), ph, kSiteK | 4);
-        if (++slot == kSlots) { slot = 0; ph ^= 1; }
+        if (++slot == kPairs) { slot = 0; ph ^= 1; }
         return r;
       };
       auto issue_s = [&](uint32_t qs) {  // S^T = K Q_i^T
@@ -551,12 +555,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(bar(DP_FULL));
       };
-      uint32_t qs = 0, ds = 0;
-      if ((ok = next_slot(qs))) issue_s(qs);
-      if (ok && (ok = next_slot(ds))) issue_dp(ds);
+      uint32_t pc = 0;
+      if ((ok = next_pair(pc))) {
+        issue_s(2 * pc);
+        issue_dp(2 * pc + 1);
+      }
       for (int i = 0; ok && i < n_q; ++i) {
         const bool more = i + 1 < n_q;
-        uint32_t qn = 0, dn = 0;
+        const uint32_t qs = 2 * pc, ds = 2 * pc + 1;
+        uint32_t pn = 0;
         // dV += P_i^T dO_i once the element-wise warps have written P_i
         if (!(ok = wait_one(bar(P_FULL), pf_ph, kSiteK | 3))) break;
         pf_ph ^= 1;
@@ -567,8 +574,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts(tbase + kTmemAcc0, tbase + kTmemS + tmem_half_col(kk), dod + ((kk * 2048) >> 4),
                  idesc_bf16_f32(128, D, true), (i > 0 || kk > 0) ? 1u : 0u);
         if (more) {
-          if (!(ok = next_slot(qn))) break;
-          issue_s(qn);
+          if (!(ok = next_pair(pn))) break;
+          issue_s(2 * pn);
         }
         // dK += dS_i^T Q_i once they have written dS_i
         if (!(ok = wait_one(bar(DS_FULL), df_ph, kSiteK | 7))) break;
@@ -579,14 +586,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < kTile / 16; ++kk)
           mma_ts(tbase + kTmemAcc1, tbase + kTmemDP + tmem_half_col(kk), qd + ((kk * 2048) >> 4),
                  idesc_bf16_f32(128, D, true), (i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(RING_EMPTY + qs));
-        mma_commit(bar(RING_EMPTY + ds));
-        if (more) {
-          if (!(ok = next_slot(dn))) break;
-          issue_dp(dn);
-        }
-        qs = qn;
-        ds = dn;
+        mma_commit(bar(RING_EMPTY + pc));  // Q_i and dO_i are free after dK_i
+        if (more) issue_dp(2 * pn + 1);
+        pc = pn;
       }
       if (ok) mma_commit(bar(O_FULL));
     }
