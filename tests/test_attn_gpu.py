@@ -131,6 +131,26 @@ def test_growing_scores(cuda_ok, causal):
 
 
 @pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_sharp_rows_within_the_p_rounding_bound(cuda_ok, causal, d):
+    """Queries scaled by 10: nearly one-hot rows whose dominant weight is not
+    a power of two against the lazy reference, so its bf16 rounding (up to
+    2^-8 relative) is not averaged away.  Bound derived from the arithmetic:
+    1e-2 + 2^-8 |O_ref| (output rounding) + 2^-8 (|P| |V|)_ref (P rounding),
+    with (|P| |V|)_ref the oracle's attention over |V|."""
+    case = W.attention(78 + d, 3, 4, 1024, 1024, d, causal, None)
+    case.q = (case.q.float() * 10.0).to(torch.bfloat16)
+    o, lse = run(case)
+    ro, rl = oracle_of(case)
+    q64, k64, av = W.as_f64(case.q), W.as_f64(case.k), np.abs(W.as_f64(case.v))
+    pv, _ = oracle.attention_ref(q64, k64, av, case.scale, case.causal, None)
+    err = np.abs(W.as_f64(o) - ro)
+    assert float(np.max(err - 2.0 ** -8 * np.abs(ro) - 2.0 ** -8 * pv)) <= O_TOL
+    fin = np.isfinite(rl)
+    assert float(np.max(np.abs(W.as_f64(lse)[fin] - rl[fin]))) <= LSE_TOL
+
+
+@pytest.mark.parametrize("causal", [False, True])
 def test_scores_far_below_zero(cuda_ok, causal):
     """Every score near -200: against the starting reference 0 all terms would
     underflow, so the first chunk of each row lowers the reference."""
