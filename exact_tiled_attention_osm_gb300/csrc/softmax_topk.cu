@@ -20,9 +20,9 @@
 // a threshold every top-k entry reaches; the second pass (served mostly from
 // L2, the slice was just read) inserts only entries that beat the warp's
 // filter into the warp's running list of 32 pairs, one per lane, and tightens
-// the filter to the list's k-th entry.  The CTA's lists
-// meet in warp 0 through shared memory and the cluster's in CTA 0 through
-// distributed shared memory, by bitonic merges.  K = 1 needs one pass
+// the filter to the list's k-th entry.  The CTA's lists meet pairwise
+// through shared memory (three rounds for eight warps) and the cluster's in
+// CTA 0 through distributed shared memory, by bitonic merges.  K = 1 needs one pass
 // (each thread's arg-max).  HBM-bound: 4 bytes read per element once from
 // HBM, 8 bytes written per output entry.
 #include <cuda_runtime.h>
@@ -189,6 +189,27 @@ __device__ __forceinline__ float warp_merge_desc(float a, float b) {
   return c;
 }
 
+
+// The CTA's warps' lane-sorted lists (s_pv/s_pi, 32 per warp) merged pairwise
+// in log2(kWarps) rounds; the result ends in warp 0's entries.  Every thread
+// of the CTA calls this (it holds the barriers).
+__device__ __forceinline__ void cta_tree_merge_pairs(float* s_pv, int* s_pi) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int step = 1; step < kWarps; step <<= 1) {
+    __syncthreads();
+    if ((warp & (2 * step - 1)) == 0) {
+      float av = s_pv[warp * 32 + lane];
+      int ai = s_pi[warp * 32 + lane];
+      warp_merge_pairs(av, ai, s_pv[(warp + step) * 32 + lane], s_pi[(warp + step) * 32 + lane]);
+      __syncwarp();
+      s_pv[warp * 32 + lane] = av;
+      s_pi[warp * 32 + lane] = ai;
+    }
+  }
+  __syncthreads();
+}
+
 // The 32 best entries over the per-thread lists of a whole cluster, lane-sorted
 // in warp 0 of CTA 0.  Warp: the lanes' r-th entries are sorted as a batch and
 // merged into the running list, one batch per list depth in use; CTA: warp 0
@@ -218,11 +239,10 @@ __device__ __forceinline__ void cluster_topk(List<K>& L, float* s_pv, int* s_pi,
   }
   s_pv[warp * 32 + lane] = av;
   s_pi[warp * 32 + lane] = ai;
-  __syncthreads();
+  cta_tree_merge_pairs(s_pv, s_pi);
   if (warp == 0) {
     av = s_pv[lane];
     ai = s_pi[lane];
-    for (int w = 1; w < kWarps; ++w) warp_merge_pairs(av, ai, s_pv[w * 32 + lane], s_pi[w * 32 + lane]);
     c_v[lane] = av;
     c_i[lane] = ai;
   }
@@ -242,11 +262,10 @@ __device__ __forceinline__ void cluster_merge_lists(float& av, int& ai, float* s
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   s_pv[warp * 32 + lane] = av;
   s_pi[warp * 32 + lane] = ai;
-  __syncthreads();
+  cta_tree_merge_pairs(s_pv, s_pi);
   if (warp == 0) {
     av = s_pv[lane];
     ai = s_pi[lane];
-    for (int w = 1; w < kWarps; ++w) warp_merge_pairs(av, ai, s_pv[w * 32 + lane], s_pi[w * 32 + lane]);
     c_v[lane] = av;
     c_i[lane] = ai;
   }
@@ -398,14 +417,19 @@ __global__ void __launch_bounds__(kThreads) softmax_topk_kernel(const float* __r
   if constexpr (K > 16) {
     // a warp's K-th lane maximum is weak for large K: also take the CTA's
     // K-th thread maximum (merged by warp 0); either bound is valid
+    // (merged pairwise in log2(kWarps) rounds)
     s_pv[warp * 32 + lane] = wsorted;
-    __syncthreads();
-    if (warp == 0) {
-      float acc = s_pv[lane];
-      for (int w = 1; w < kWarps; ++w) acc = warp_merge_desc(acc, s_pv[w * 32 + lane]);
-      const float t = __shfl_sync(0xffffffffu, acc, K - 1);
-      if (lane == 0) c_ml[0] = t;  // staged here until the summary is written
+#pragma unroll
+    for (int step = 1; step < kWarps; step <<= 1) {
+      __syncthreads();
+      if ((warp & (2 * step - 1)) == 0) {
+        const float acc = warp_merge_desc(s_pv[warp * 32 + lane], s_pv[(warp + step) * 32 + lane]);
+        __syncwarp();
+        s_pv[warp * 32 + lane] = acc;
+      }
     }
+    __syncthreads();
+    if (warp == 0 && lane == 0) c_ml[0] = s_pv[K - 1];  // staged until the summary is written
     __syncthreads();
     thr = fmaxf(thr, c_ml[0]);
   }
