@@ -42,6 +42,7 @@ using namespace ptx;
 constexpr int kTile = 128;   // rows of every tile (query or key)
 constexpr int kSlots = 4;    // streamed 32 KB tiles in flight
 constexpr int kPairs = kSlots / 2;  // dK/dV kernel: the slots as (Q_i, dO_i) pairs
+constexpr uint32_t kKSlots = 3, kVSlot = 3;  // dQ kernel: K tiles in slots 0-2, V in slot 3
 constexpr uint32_t kTileBytes = kTile * 128 * 2;  // 32768: a slot holds a d = 128 tile
 constexpr uint32_t kBoxBytes = 128 * 64 * 2;           // one TMA box: 64 columns x 128 rows
 constexpr int kThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 4-11 element-wise
@@ -238,20 +239,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_3d(sQ + c * kBoxBytes, &tm_q, bar(RES_FULL), c * 64, q0, bh);
       tma_load_3d(sDO + c * kBoxBytes, &tm_do, bar(RES_FULL), c * 64, q0, bh);
     }
-    uint32_t slot = 0, ph = 0, fill_mask = 0, fill_ph = 0;
+    // K tiles through slots 0-2 and V tiles through slot 3, loaded in the
+    // order K_0, V_0, K_1, then (K_{j+2}, V_{j+1}) for j = 0, 1, ...: K_j is
+    // read by S_j (issued in step j-1) and by dQ_j (step j), V_j only by dP_j,
+    // so three K slots let K_{j+2} load while step j-1 runs.
+    uint32_t kslot = 0, kph = 0, vph = 0, fill_mask = 0, fill_ph = 0;
     bool ok = true;
-    for (int j = 0; ok && j < n_kv; ++j) {
-      for (int kv = 0; kv < 2; ++kv) {  // K_j then V_j
-        if (!(ok = wait_one(bar(RING_EMPTY + slot), ph ^ 1, kSiteQ | 1))) break;
-        mbar_arrive_expect_tx(bar(RING_FULL + slot), kTile * D * 2);
-        const CUtensorMap* tm = kv ? &tm_v : &tm_k;
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sRing + slot * kTileBytes + c * kBoxBytes, tm, bar(RING_FULL + slot), c * 64,
-                      j * kTile, bh);
-        fill_mask |= 1u << slot;
-        fill_ph = (fill_ph & ~(1u << slot)) | (ph << slot);
-        if (++slot == kSlots) { slot = 0; ph ^= 1; }
-      }
+    auto load = [&](uint32_t sl, uint32_t phs, const CUtensorMap* tm, int j) -> bool {
+      if (!wait_one(bar(RING_EMPTY + sl), phs ^ 1, kSiteQ | 1)) return false;
+      mbar_arrive_expect_tx(bar(RING_FULL + sl), kTile * D * 2);
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_3d(sRing + sl * kTileBytes + c * kBoxBytes, tm, bar(RING_FULL + sl), c * 64,
+                    j * kTile, bh);
+      fill_mask |= 1u << sl;
+      fill_ph = (fill_ph & ~(1u << sl)) | (phs << sl);
+      return true;
+    };
+    auto load_k = [&](int j) -> bool {
+      const bool r = load(kslot, kph, &tm_k, j);
+      if (++kslot == kKSlots) { kslot = 0; kph ^= 1; }
+      return r;
+    };
+    auto load_v = [&](int j) -> bool {
+      const bool r = load(kVSlot, vph, &tm_v, j);
+      vph ^= 1;
+      return r;
+    };
+    if (n_kv > 0) ok = load_k(0) && load_v(0);
+    if (ok && n_kv > 1) ok = load_k(1);
+    for (int j = 0; ok && j + 1 < n_kv; ++j) {
+      if (j + 2 < n_kv) ok = load_k(j + 2);
+      if (ok) ok = load_v(j + 1);
     }
     if (!ok) {  // let every copy this thread started land before the CTA exits
       for (int s = 0; s < kSlots; ++s)
@@ -267,14 +285,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dKm = sdesc_sw128(0, 16, 1024);      // K-major template
     const uint64_t dMN = sdesc_sw128(0, 16384, 1024);   // MN-major template
     bool ok = wait_one(bar(RES_FULL), 0, kSiteQ | 2);
-    uint32_t slot = 0, ph = 0, df_ph = 0;
+    uint32_t kslot = 0, kph = 0, vph = 0, df_ph = 0;
     if (ok) {
       tc_fence_after();
       const uint64_t qdesc = dKm + (sQ >> 4), dodesc = dKm + (sDO >> 4);
-      auto next_slot = [&](uint32_t& s_out) -> bool {  // ring slots in fill order
-        s_out = slot;
-        const bool r = wait_one(bar(RING_FULL + slot), ph, kSiteQ | 4);
-        if (++slot == kSlots) { slot = 0; ph ^= 1; }
+      auto next_k = [&](uint32_t& s_out) -> bool {  // K slots in fill order
+        s_out = kslot;
+        const bool r = wait_one(bar(RING_FULL + kslot), kph, kSiteQ | 4);
+        if (++kslot == kKSlots) { kslot = 0; kph ^= 1; }
+        return r;
+      };
+      auto next_v = [&](uint32_t& s_out) -> bool {
+        s_out = kVSlot;
+        const bool r = wait_one(bar(RING_FULL + kVSlot), vph, kSiteQ | 4);
+        vph ^= 1;
         return r;
       };
       auto issue_s = [&](uint32_t ks, int jj) {  // S_jj = Q K_jj^T into buffer jj & 1
@@ -300,13 +324,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar(RING_EMPTY + vs));
       };
       uint32_t ks = 0, vs = 0;
-      if ((ok = next_slot(ks))) issue_s(ks, 0);
-      if (ok && (ok = next_slot(vs))) issue_dp(vs);
+      if ((ok = next_k(ks))) issue_s(ks, 0);
+      if (ok && (ok = next_v(vs))) issue_dp(vs);
       for (int j = 0; ok && j < n_kv; ++j) {
         const bool more = j + 1 < n_kv;
         uint32_t kn = 0;
         if (more) {
-          if (!(ok = next_slot(kn))) break;
+          if (!(ok = next_k(kn))) break;
           issue_s(kn, j + 1);
         }
         // dQ += dS_j K_j once the element-wise warps have written dS_j
@@ -321,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                  (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(RING_EMPTY + ks));  // K_j is free after this product
         if (more) {
-          if (!(ok = next_slot(vs))) break;
+          if (!(ok = next_v(vs))) break;
           issue_dp(vs);
         }
         ks = kn;
