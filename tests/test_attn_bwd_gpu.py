@@ -3,13 +3,13 @@
 Inputs: q, k, v, dO bf16; O (rounded to bf16) and lse (fp32) from the
 oracle's own forward, so nothing fed to either side comes from the CUDA path.
 Bar, element by element, derived from the kernel's arithmetic: P and dS are
-rounded to bf16 (relative error <= 2^-9) before the products that use them,
-and the outputs are stored in bf16, so
+rounded to bf16 (unit roundoff 2^-8) before the products that use them, and
+the outputs are stored in bf16 (another 2^-8 relative), so
   |dV - dV_ref| <= 2^-8 (|P|^T |dO|) + 2^-8 |dV_ref| + 1e-4,
   |dQ - dQ_ref| <= 2^-8 scale (|dS| |K|) + 2^-8 |dQ_ref| + 1e-4,
   |dK - dK_ref| <= 2^-8 scale (|dS|^T |Q|) + 2^-8 |dK_ref| + 1e-4
-(twice the first-order rounding terms; the fp32 accumulation and exp2 error
-are below the absolute term).
+(the first term is the P / dS rounding with every error aligned; the fp32
+accumulation and exp2 error are below the absolute term).
 """
 import numpy as np
 import pytest
