@@ -6,6 +6,8 @@ Bar (BF16 inputs, float64 oracle on the same bf16-rounded inputs):
   LSE: |lse_gpu - lse_ref| <= 1e-3, and -inf exactly where the oracle has -inf;
   masked keys contribute exactly zero (bitwise test across two paddings).
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -264,6 +266,17 @@ def test_very_long_sequence(cuda_ok):
     o, lse = run(cross)
     ro, rl = oracle_of(cross)
     check(o, lse, ro, rl)
+
+
+def test_many_small_heads(cuda_ok):
+    """B·H = 16384 heads of 100 queries and keys (one ragged 128-wide tile
+    each): 16384 work items over the persistent grid, causal, d = 64."""
+    B, H, N, d = 4096, 4, 100, 64
+    g = torch.Generator().manual_seed(94)  # one draw for all heads (fast at this count)
+    q, k, v = (torch.randn(B, H, N, d, generator=g).to(torch.bfloat16) for _ in range(3))
+    case = W.AttnCase(q, k, v, 1.0 / math.sqrt(d), True, None)
+    o, lse = run(case)
+    check(o, lse, *oracle_of(case))
 
 
 def test_cross_attention_shapes(cuda_ok):

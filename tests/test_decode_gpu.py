@@ -73,6 +73,22 @@ def test_small_ragged(cuda_ok, dtype, d, splits):
     assert torch.all(o[0] == 0) and torch.all(torch.isneginf(lse[0]))
 
 
+def test_largest_grid(cuda_ok):
+    """B = 65535 (the largest batch the decode grid takes), one head, short
+    ragged caches, 3 splits: every row against the oracle."""
+    B, H, Nk, d = 65535, 1, 40, 64
+    g = torch.Generator().manual_seed(36)  # one draw for all rows (fast at this batch)
+    q = torch.randn(B, H, 1, d, generator=g).to(torch.bfloat16)
+    k = torch.randn(B, H, Nk, d, generator=g).to(torch.bfloat16)
+    v = torch.randn(B, H, Nk, d, generator=g).to(torch.bfloat16)
+    kl = torch.randint(0, Nk + 1, (B,), generator=g, dtype=torch.int32)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = osm.attn_decode_splitkv(q.cuda(), k.cuda(), v.cuda(), scale, kl.cuda(), 3)
+    assert osm.device_status() == 0
+    ro, rl = ref_decode(q, k, v, scale, kl)
+    check_bf16(o, lse, ro, rl)
+
+
 def test_partials_in_workspace(cuda_ok):
     B, H, Nk, d, S = 3, 2, 2000, 128, 16
     case = W.decode(seed=40, B=B, H=H, Nk=Nk, d=d, len_range=(5, Nk), num_splits=S)
