@@ -16,7 +16,8 @@
 //   work item  = (b, h, pair of 128-row query tiles); both tiles share every
 //                streamed K/V tile, and alternate on the tensor core so one
 //                tile's softmax overlaps the other tile's matrix products.
-//   warp 0     TMA producer: Q tiles once per item, then K_j together with
+//   warp 0     TMA producer: Q tiles once per item (and an L2 prefetch of the
+//              next item's Q as soon as its number is known), then K_j together with
 //              V_{j-1} (the two tiles step j reads) into one of two pairs of
 //              shared-memory slots (128-byte swizzle) under one mbarrier, so
 //              each key step costs the MMA thread one wait and one release.
@@ -31,7 +32,9 @@
 //              TMEM -> registers, mask, scale and subtract the reference in
 //              packed f32x2, independent exp2 (so the MUFU latency is
 //              covered), row sum, bf16 pack, store P over the S columns
-//              already consumed; epilogue O = O~ / l, lse.
+//              already consumed; epilogue O = O~ / l (staged per warp in
+//              shared memory so that global stores cover whole 64-byte row
+//              segments), lse.
 //   TMEM       512 columns: S_0 | S_1 | O~_0 | O~_1 (128 fp32 columns each).
 // The reference subtracted before exp2 need not be the running maximum: every
 // identity of the recurrence holds for any common reference ("Precision, and
@@ -94,7 +97,11 @@ enum Bar : uint32_t {
 constexpr uint32_t kSmemTmemSlot = kSmemBar + 8 * NUM_BARS;
 constexpr uint32_t kSmemAbort = kSmemTmemSlot + 4;
 constexpr uint32_t kSmemItems = kSmemAbort + 4;  // int[kItemSlots]: the CTA's item queue
-constexpr uint32_t kSmemBytes = kSmemItems + 4 * kItemSlots + 1024;  // + alignment slack
+// per softmax warp: one 32-column chunk of its 32 output rows (bf16), staged
+// so that the warp's global stores cover whole 64-byte row segments
+constexpr uint32_t kStageBytes = 32 * 64;
+constexpr uint32_t kSmemStage = (kSmemItems + 4 * kItemSlots + 127) / 128 * 128;
+constexpr uint32_t kSmemBytes = kSmemStage + 8 * kStageBytes + 1024;  // + alignment slack
 // readers of the item queue: the MMA thread and the eight softmax warps
 constexpr uint32_t kItemReaders = 1 + 8;
 
@@ -152,6 +159,15 @@ __device__ __forceinline__ void mma_ts_x8(uint32_t d, uint32_t a, uint64_t b, ui
       " tcgen05.mma.cta_group::1.kind::f16 [%0], [t7], b7, %3, p1;\n}\n" ::"r"(d),
       "r"(a), "l"(b), "r"(idesc), "r"(acc0)
       : "memory");
+}
+
+
+// Bring a 3-D tile into L2 ahead of its load (no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
 }
 
 struct Params {
@@ -296,6 +312,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           published = true;
           const int64_t nx = static_cast<int64_t>(gridDim.x) + ticket;
           item = nx < p.num_items ? static_cast<int>(nx) : -1;
+          if (item >= 0) {  // the next item's Q into L2 while this one runs
+            const Item nit = item_info(p, item);
+            if (nit.n_kv > 0)
+              for (int t = 0; t < 2 && nit.q0 + t * kRows < p.Nq; ++t)
+                for (int c = 0; c < D / 64; ++c)
+                  tma_prefetch_l2_3d(&tm_q, c * 64, nit.q0 + t * kRows, nit.bh);
+          }
           return publish(item);
         };
         if (it.n_kv > 0) {
@@ -642,23 +665,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       of_ph ^= 1;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll
+      // O = O~ / l in bf16, a 32-column chunk at a time: each thread puts its
+      // row's 64 bytes into the warp's staging area, then the warp stores 8
+      // rows x 64 contiguous bytes per instruction (4 lanes per row segment)
+      uint4* stage = reinterpret_cast<uint4*>(smem + kSmemStage + (warp - 4) * kStageBytes);
+      const int srow = (lane >> 2);  // this lane's row within each group of 8
+      const int64_t orow0 = static_cast<int64_t>(it.bh) * p.Nq + (row - lane);
+#pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t orr[32];
         tmem_ld_x32(tO + 32 * c, orr);
-        if (row_ok) {
-          uint32_t pk2[16];
+        uint32_t pk2[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(orr[2 * e]) * inv,
-                                                      __uint_as_float(orr[2 * e + 1]) * inv);
-            pk2[e] = *reinterpret_cast<uint32_t*>(&h2);
-          }
-          uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D + 32 * c);
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            dst[e] = make_uint4(pk2[4 * e], pk2[4 * e + 1], pk2[4 * e + 2], pk2[4 * e + 3]);
+        for (int e = 0; e < 16; ++e) {
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(orr[2 * e]) * inv,
+                                                    __uint_as_float(orr[2 * e + 1]) * inv);
+          pk2[e] = *reinterpret_cast<uint32_t*>(&h2);
         }
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          stage[lane * 4 + e] = make_uint4(pk2[4 * e], pk2[4 * e + 1], pk2[4 * e + 2], pk2[4 * e + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int r = 8 * g + srow;  // row of the warp this lane stores
+          if (row - lane + r < p.Nq) {
+            uint4* dst = reinterpret_cast<uint4*>(p.o + (orow0 + r) * D + 32 * c);
+            dst[lane & 3] = stage[r * 4 + (lane & 3)];
+          }
+        }
+        __syncwarp();
       }
       tc_fence_before();
       __syncwarp();
