@@ -42,8 +42,8 @@ ATTN_SRC = os.path.join(ROOT, "exact_tiled_attention_osm_gb300", "csrc", "attn_f
 # DRAM traffic of one attention launch on this workload from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
 # source it was captured on (sha256 of attn_fwd.cu); None until captured.
-ATTN_TRAFFIC = {"bytes_per_launch": 1_260_000_000 + 517_450_000,
-                "source_sha256": "5a7a2094039f30d4005afcd18e3f6b28e22711d07c271cb25aa24a195ac154ce"}
+ATTN_TRAFFIC = {"bytes_per_launch": 1_330_000_000 + 519_670_000,
+                "source_sha256": "a5492fc1fa1c47ee81e318f62bd0e28ee5a0cc3951bb02647e222fb7ba5d4736"}
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
