@@ -77,7 +77,11 @@ constexpr uint32_t kSmemAbort = kSmemTmemSlot + 4;
 // per softmax warp: [2 buffers][lse2 | D][128 columns] floats
 constexpr uint32_t kSmemCol = (kSmemAbort + 4 + 15) / 16 * 16;
 constexpr uint32_t kColFloats = 2 * 2 * (kTile / 2);
-constexpr uint32_t kSmemBytes = kSmemCol + 8 * kColFloats * 4 + 1024;
+// per element-wise warp: one 32-column chunk of its 32 output rows (bf16),
+// staged so that the warp's global stores cover whole 64-byte row segments
+constexpr uint32_t kStageBytes = 32 * 64;
+constexpr uint32_t kSmemStage = (kSmemCol + 8 * kColFloats * 4 + 127) / 128 * 128;
+constexpr uint32_t kSmemBytes = kSmemStage + 8 * kStageBytes + 1024;
 
 constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemAcc0 = 256, kTmemAcc1 = 384;
 
@@ -109,25 +113,39 @@ __host__ __device__ constexpr uint32_t tmem_half_col(int kk) {
   return static_cast<uint32_t>(64 * (kk >> 2) + 8 * (kk & 3));
 }
 
-// 16-byte global stores of 32-column chunks c0 .. c1-1 of one bf16 row from TMEM
-__device__ __forceinline__ void store_row_bf16(uint32_t t_acc, float mul, __nv_bfloat16* dst,
-                                               bool ok, int c0 = 0, int c1 = 4) {
+// The warp's 32 rows of a bf16 output (row r at base + r * D), 32-column
+// chunks c0 .. c1-1 read from TMEM and scaled by mul: each thread puts its
+// row's 64 bytes of a chunk into the warp's staging area, then the warp stores
+// 8 rows x 64 contiguous bytes per instruction.  Rows from nvalid on are not
+// stored.
+template <int D>
+__device__ __forceinline__ void store_rows_bf16_staged(uint32_t t_acc, float mul,
+                                                       __nv_bfloat16* base, int nvalid, int c0,
+                                                       int c1, uint4* stage) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll 1
   for (int c = c0; c < c1; ++c) {
     uint32_t r[32];
     tmem_ld_x32(t_acc + 32 * c, r);
-    if (ok) {
-      uint32_t pk[16];
+    uint32_t pk[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(r[2 * e]) * mul,
-                                                  __uint_as_float(r[2 * e + 1]) * mul);
-        pk[e] = *reinterpret_cast<uint32_t*>(&h2);
-      }
-      uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+    for (int e = 0; e < 16; ++e) {
+      __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(r[2 * e]) * mul,
+                                                __uint_as_float(r[2 * e + 1]) * mul);
+      pk[e] = *reinterpret_cast<uint32_t*>(&h2);
     }
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      stage[lane * 4 + e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const int rr = 8 * g + (lane >> 2);
+      if (rr < nvalid)
+        reinterpret_cast<uint4*>(base + static_cast<int64_t>(rr) * D + 32 * c)[lane & 3] =
+            stage[rr * 4 + (lane & 3)];
+    }
+    __syncwarp();
   }
 }
 
@@ -426,9 +444,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) ok = __all_sync(0xffffffffu, wait_one(bar(O_FULL), 0, kSiteQ | 6));
     if (ok) {
       tc_fence_after();
-      store_row_bf16(tbase + lane_off + kTmemAcc0, p.scale,
-                     p.dq + (static_cast<int64_t>(bh) * p.Nq + row) * D, row_ok,
-                     hh * (D / 64), (hh + 1) * (D / 64));
+      const int row0 = row - lane;  // the warp's first query row
+      store_rows_bf16_staged<D>(
+          tbase + lane_off + kTmemAcc0, p.scale,
+          p.dq + (static_cast<int64_t>(bh) * p.Nq + row0) * D, min(32, p.Nq - row0),
+          hh * (D / 64), (hh + 1) * (D / 64),
+          reinterpret_cast<uint4*>(smem + kSmemStage + (warp - 4) * kStageBytes));
     }
   }
   tc_fence_before();
@@ -741,12 +762,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) ok = __all_sync(0xffffffffu, wait_one(bar(O_FULL), 0, kSiteK | 6));
     if (ok) {
       tc_fence_after();
-      const bool st_ok = key < p.Nk;
-      const int64_t g = (static_cast<int64_t>(bh) * p.Nk + (st_ok ? key : 0)) * D;
+      const int key0 = key - lane;  // the warp's first key row
+      const int64_t g = (static_cast<int64_t>(bh) * p.Nk + key0) * D;
+      uint4* stage = reinterpret_cast<uint4*>(smem + kSmemStage + (warp - 4) * kStageBytes);
       if (hh == 0)
-        store_row_bf16(tbase + lane_off + kTmemAcc0, 1.f, p.dv + g, st_ok, 0, D / 32);
+        store_rows_bf16_staged<D>(tbase + lane_off + kTmemAcc0, 1.f, p.dv + g,
+                                  min(32, p.Nk - key0), 0, D / 32, stage);
       else
-        store_row_bf16(tbase + lane_off + kTmemAcc1, p.scale, p.dk + g, st_ok, 0, D / 32);
+        store_rows_bf16_staged<D>(tbase + lane_off + kTmemAcc1, p.scale, p.dk + g,
+                                  min(32, p.Nk - key0), 0, D / 32, stage);
     }
   }
   tc_fence_before();
