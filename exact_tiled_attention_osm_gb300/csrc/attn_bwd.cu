@@ -12,18 +12,21 @@
 // Three kernels:
 //   bwd_delta_kernel  D = rowsum(dO * O), fp32 (HBM-bound).
 //   bwd_dq_kernel     one CTA per (b, h, 128-query tile); streams the visible
-//                     K/V tiles.  S = Q K^T and dP = dO V^T into TMEM; one
-//                     thread per query row forms P and dS (its lse and D stay
-//                     in registers) and writes dS as bf16 over the S columns;
+//                     K tiles (three slots) and V tiles (one slot).  S = Q K^T
+//                     and dP = dO V^T into TMEM; two threads per query row
+//                     (each half the columns) form P and dS (lse and D in
+//                     registers) and write dS as bf16 over the S columns;
 //                     dQ += dS K with dS read straight from TMEM.
-//   bwd_dkdv_kernel   one CTA per (b, h, 128-key tile); streams the query
-//                     tiles that see it.  S^T = K Q^T and dP^T = V dO^T into
-//                     TMEM; one thread per key row forms P^T and dS^T (lse and
-//                     D per column from shared memory) and writes both as bf16
-//                     over S^T and dP^T; dV += P^T dO and dK += dS^T Q read
-//                     them straight from TMEM.
+//   bwd_dkdv_kernel   one CTA per (b, h, 128-key tile); streams (Q_i, dO_i)
+//                     pairs for the query tiles that see it.  S^T = K Q^T and
+//                     dP^T = V dO^T into TMEM; two threads per key row form
+//                     P^T and dS^T (lse and D per column from shared memory)
+//                     and write both as bf16 over S^T and dP^T; dV += P^T dO
+//                     and dK += dS^T Q read them straight from TMEM.
 // dQ and dK/dV are separate so that no partial sum crosses CTAs (no atomics);
-// the price is S and dP formed twice (7 instead of 5 matrix products).
+// the price is S and dP formed twice (7 instead of 5 matrix products).  The
+// outputs leave through a per-warp shared-memory stage so that every store
+// covers whole 64-byte row segments.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
