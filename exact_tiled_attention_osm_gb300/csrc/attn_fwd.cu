@@ -41,9 +41,12 @@
 // what can still go wrong", second point: any bound on the scores will do).
 // So only a row's first tile looks for the maximum (or none, when the caller
 // knows a bound and the row starts there).  After that the reference moves by
-// whole binades only when a chunk would otherwise hold a term above 2^16
-// (raise: everything formed so far is scaled by an exact power of two) or
-// when all of a row's terms so far underflow (lower).
+// whole binades when a chunk would otherwise hold a term above 2^16 (raise:
+// everything formed so far is scaled by an exact power of two) or when all of a
+// row's terms so far underflow (lower), and to a chunk's exact maximum when
+// that chunk outweighs everything before it in the row: a row's dominant term
+// then has weight exactly 1, which its bf16 rounding for the P V product leaves
+// unchanged, so a nearly one-hot row returns its value's bf16 bits.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -71,8 +74,9 @@ constexpr int kThreads = 384;
 // A 32-term chunk whose sum stays at or below kSumLimit has no term above it
 // (all terms are >= 0), so every P is at most 2^16 times the reference's term.
 constexpr float kSumLimit = 65536.0f;
-// A row's first tile may leave the reference up to kTau below the maximum.
-constexpr float kTau = 8.0f;
+// The most a dominant chunk may lower a caller's bound (binades), so that the
+// scale 2^k applied to what the row has accumulated stays finite in FP32.
+constexpr float kMaxLower = 120.0f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNegInf = -__builtin_huge_valf();
 
@@ -496,9 +500,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // that a row's first tile takes its maximum, or a bound the caller
       // knows.  Later tiles form their terms against the current reference
       // without looking for the maximum: a chunk with a term that may exceed
-      // kSumLimit raises the reference, a chunk whose terms all underflow
-      // while nothing has accumulated yet lowers it.
-      float m_ref = kBounded ? p.m_init : kNegInf, l = 0.f;
+      // kSumLimit raises the reference, a chunk that outweighs the row so far
+      // moves it to the chunk's maximum, and a chunk whose terms all
+      // underflow while nothing has accumulated yet lowers it.
+      // l: the row's sum of FP32 terms (it gives the lse); lrun: the same sum up
+      // to the current chunk (decides which chunk dominates the row); corr
+      // (known bound only): the bf16 rounding of the first tile's terms, which
+      // start at the caller's bound rather than at a maximum -- O is divided by
+      // l + corr, so those terms weigh O exactly as the tensor core used them.
+      float m_ref = kBounded ? p.m_init : kNegInf, l = 0.f, lrun = 0.f, corr = 0.f;
+      bool at_bound = kBounded;  // the reference is still the caller's bound
       for (int j = 0; j < it.n_kv; ++j) {
         ok = wait_all(bar(S_FULL + t), sf_ph, kSite | 7);
         if (!ok) break;
@@ -532,9 +543,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           bool resc = false;
           if (m_ref == kNegInf) {
             m_ref = m_new;
-          } else if (m_new > m_ref + kTau) {
+          } else if (m_new > m_ref) {  // the tile's maximum becomes the reference exactly
             alpha = ex2(m_ref - m_new);
             l *= alpha;
+            lrun *= alpha;
             m_ref = m_new;
             resc = true;
           }
@@ -556,6 +568,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr int kCw = (D == 64 || kBounded) ? 64 : 32;
         constexpr int kNch = kKeys / kCw;
         float la[4] = {0.f, 0.f, 0.f, 0.f};
+        // a chunk whose sum passes thr moves the reference (see below)
+        float thr = j > 0 ? fminf(lrun, kSumLimit) : kSumLimit;
 #pragma unroll 1
         for (int ch = 0; ch < kNch; ++ch) {
           uint32_t v[kCw], pk[kCw / 2];
@@ -586,37 +600,55 @@ __global__ void __launch_bounds__(kThreads, 1)
           };
           load_chunk();
           exp_chunk();
+          float csum = (cs[0] + cs[1]) + (cs[2] + cs[3]);
           if (!first) {
-            bool over = !((cs[0] + cs[1]) + (cs[2] + cs[3]) <= kSumLimit);
-            if constexpr (kBounded)  // every term underflowed and nothing has accumulated
-              over = over || ((cs[0] + cs[1]) + (cs[2] + cs[3]) == 0.f && l == 0.f &&
-                              (la[0] + la[1]) + (la[2] + la[3]) == 0.f);
-            if (__any_sync(0xffffffffu, over)) {
-              // Move the reference by a whole number k of binades so that this
-              // chunk's largest term is 1.  Raising (k > 0) multiplies
-              // everything already formed against the old reference (l, the
-              // stored P chunks, O~) by 2^-k, which is exact.  Lowering (only
-              // with a caller's bound) happens while nothing has accumulated.
+            // Three reasons to move the reference.  over: a term may exceed
+            // kSumLimit.  dom: the chunk outweighs everything before it in the
+            // row, so it may hold the row's dominant term -- that term gets an
+            // exact reference (its weight becomes exactly 1, which bf16
+            // represents, so O is not off by that weight's rounding).  under
+            // (caller's bound only): every term so far underflowed.  Over and
+            // dom are one comparison against thr (NaN fails it as well).
+            bool any = !(csum <= thr);
+            if constexpr (kBounded) any = any || (csum == 0.f && lrun == 0.f);
+            if (__any_sync(0xffffffffu, any)) {
+              const bool over = !(csum <= kSumLimit);
+              const bool dom = j > 0 && csum > lrun;
+              const bool under = kBounded && csum == 0.f && lrun == 0.f;
               // The chunk's scores are still in TMEM (P of earlier chunks lies
               // in lower columns): read them again.
               load_chunk();
-              float kr = 0.f;
-              if (over) {
-                float mc = kNegInf;
+              float mc = kNegInf;
 #pragma unroll
-                for (int e = 0; e < kCw; ++e) mc = fmaxf(mc, __uint_as_float(v[e]));
-                if constexpr (kBounded) {
-                  if (mc != kNegInf) kr = ceilf(fmaf(mc, sl2, nref));
-                } else {
-                  kr = fmaxf(ceilf(fmaf(mc, sl2, nref)), 0.f);
+              for (int e = 0; e < kCw; ++e) mc = fmaxf(mc, __uint_as_float(v[e]));
+              float m_new = m_ref, alpha = 1.f;
+              if (mc != kNegInf) {
+                const float mx = mc * sl2;  // the chunk's maximum, base-2 units
+                if (dom && (mx > m_ref || (kBounded && at_bound))) {
+                  // exact reference: everything formed so far is scaled by
+                  // 2^(m_ref - mx), l, O~ and the stored P alike
+                  m_new = kBounded ? fmaxf(mx, m_ref - kMaxLower) : mx;
+                  if (lrun > 0.f) alpha = ex2(m_ref - m_new);
+                  at_bound = false;
+                } else if (over || under) {
+                  // a whole number k of binades, so that the chunk's largest
+                  // term is at most 1: raising (k > 0) scales everything formed
+                  // so far by 2^-k, exactly; lowering (caller's bound only)
+                  // happens while nothing has accumulated
+                  float kr = ceilf(fmaf(mc, sl2, nref));
+                  if constexpr (!kBounded) kr = fmaxf(kr, 0.f);
+                  m_new = m_ref + kr;
+                  // 2^-k exactly; k >= 127 leaves nothing representable (flush to 0)
+                  alpha = (kBounded && kr <= 0.f)
+                              ? 1.f
+                              : (kr >= 127.f ? 0.f : __int_as_float((127 - static_cast<int>(kr)) << 23));
                 }
               }
-              // 2^-k exactly; k >= 127 leaves nothing representable (flush to 0)
-              const float alpha = (kBounded && kr <= 0.f) ? 1.f
-                                  : (kr >= 127.f ? 0.f : __int_as_float((127 - static_cast<int>(kr)) << 23));
-              m_ref += kr;
+              m_ref = m_new;
               nref = -m_ref;
               l *= alpha;
+              lrun *= alpha;
+              corr *= alpha;
 #pragma unroll
               for (int i = 0; i < 4; ++i) la[i] *= alpha;
               tmem_wait_st();
@@ -645,6 +677,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st_x32(tO + 32 * c, orr);
               }
               exp_chunk();
+              csum = (cs[0] + cs[1]) + (cs[2] + cs[3]);
+            }
+          }
+          lrun += csum;
+          thr = j > 0 ? fminf(lrun, kSumLimit) : kSumLimit;  // for the next chunk
+          if constexpr (kBounded) {
+            if (j == 0) {  // the first tile's terms as rounded to bf16
+              float h0 = 0.f, h1 = 0.f;
+#pragma unroll
+              for (int i = 0; i < kCw / 2; ++i)
+                add2(h0, h1, __uint_as_float(pk[i] << 16), __uint_as_float(pk[i] & 0xffff0000u));
+              corr += (h0 + h1) - csum;
             }
           }
 #pragma unroll
@@ -664,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       of_ph ^= 1;
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l + corr > 0.f ? 1.f / (l + corr) : 0.f;
       // O = O~ / l in bf16, a 32-column chunk at a time: each thread puts its
       // row's 64 bytes into the warp's staging area, then the warp stores 8
       // rows x 64 contiguous bytes per instruction (4 lanes per row segment)

@@ -384,27 +384,61 @@ cudaError_t launch_decode_splitkv(osm_dtype dt, const void* q, const void* k, co
 // split summaries kept in this fixed-size device array instead of a workspace
 // of their own.  Host code must not hand the array's name to a kernel (on the
 // host it is only a stand-in symbol, not a device address): the device
-// address is looked up once per device with cudaGetSymbolAddress and cached.
+// address is looked up with cudaGetSymbolAddress once per device and context
+// and cached together with the context's unique id, so a new context on the
+// device (after cudaDeviceReset, say) is seen and the address looked up again.
 namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[OSM_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxCachedDevices = 64;
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[kMaxCachedDevices] = {};
+unsigned long long g_noalloc_ctx[kMaxCachedDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// The unique id of the calling thread's current context (0 if unknown).
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
 
 cudaError_t noalloc_scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  const bool cacheable = dev >= 0 && dev < kMaxCachedDevices;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (dev >= 0 && dev < kMaxCachedDevices && g_noalloc_ptr[dev] != nullptr) {
+  const unsigned long long ctx = current_context_id();
+  if (cacheable && ctx != 0 && g_noalloc_ptr[dev] != nullptr && g_noalloc_ctx[dev] == ctx) {
     *out = g_noalloc_ptr[dev];
     return cudaSuccess;
   }
   void* p = nullptr;
   e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // the current device's copy
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < kMaxCachedDevices) g_noalloc_ptr[dev] = p;
+  if (cacheable) {
+    g_noalloc_ptr[dev] = p;
+    g_noalloc_ctx[dev] = current_context_id();  // the context now exists
+  }
   *out = p;
   return cudaSuccess;
 }

@@ -275,8 +275,11 @@ osm_status osm_lse_merge(const float *o_parts, const float *lse_parts, int S, in
  * osm_attn_decode_splitkv_workspace_bytes(B, H, d, num_splits) is larger.
  *
  * The first call on a device looks up the scratch area's device address
- * (with that device current) and caches it; make that first call before any
- * stream capture begins.
+ * (with that device current) and caches it with the id of the device's
+ * current context; make that first call before any stream capture begins.
+ * A call that finds a different context current (after cudaDeviceReset, or
+ * under a context the caller created) looks the address up again, so it too
+ * should come before any capture.
  * Every call on a device shares the one scratch area, which keeps the last
  * call's summaries; nothing in it needs to start at zero, because the split
  * kernel writes every summary slot that the merge kernel reads.  Calls whose

@@ -1,8 +1,9 @@
 """Attention forward on the GPU against the float64 oracle.
 
-Bar (BF16 inputs, float64 oracle on the same bf16-rounded inputs):
-  O:   |O_gpu - O_ref| <= 1e-2 + 2^-8 |O_ref|   — 1e-2 on the value, plus the
-       output's own bf16 storage rounding (at most half a bf16 ulp <= 2^-8 |O|);
+Bars (``bars.py``; BF16 inputs, float64 oracle on the same bf16-rounded inputs):
+  O:   |O_gpu - O_ref| <= 1e-2 on every element of the full-size workloads;
+       elsewhere <= 1e-2 + 2^-8 |O_ref| (1e-2 on the value before the output's
+       own bf16 storage rounding, which alone can reach 2^-8 |O|);
   LSE: |lse_gpu - lse_ref| <= 1e-3, and -inf exactly where the oracle has -inf;
   masked keys contribute exactly zero (bitwise test across two paddings).
 """
@@ -15,22 +16,13 @@ import torch
 import exact_tiled_attention_osm_gb300 as osm
 import oracle
 import workloads as W
+from bars import check_attention, record
 
 pytestmark = pytest.mark.gpu
 
-O_TOL, O_REL, LSE_TOL = 1e-2, 2.0 ** -8, 1e-3
-
 
 def check(o, lse, ro, rl):
-    o, lse = W.as_f64(o), W.as_f64(lse)
-    assert np.array_equal(np.isneginf(lse), np.isneginf(rl)), "masked-row pattern differs"
-    fin = np.isfinite(rl)
-    err_o = np.abs(o - ro)
-    assert np.all(np.isfinite(o))
-    assert float(np.max(err_o - O_REL * np.abs(ro))) <= O_TOL, f"O err {err_o.max()}"
-    if fin.any():
-        assert float(np.max(np.abs(lse[fin] - rl[fin]))) <= LSE_TOL
-    return float(err_o.max())
+    return check_attention(W.as_f64(o), W.as_f64(lse), ro, rl, plain)
 
 
 def run(case, dev="cuda"):
@@ -129,27 +121,52 @@ def test_growing_scores(cuda_ok, causal):
     k[1, 1, 300:310] *= 25.0  # a block of large keys mid-row
     case.k = k.to(torch.bfloat16)
     o, lse = run(case)
-    check(o, lse, *oracle_of(case))
+    eo, el = check(o, lse, *oracle_of(case))
+    record(f"growing scores causal={causal}", o_err=eo, lse_err=el)
 
 
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("d", [64, 128])
-def test_sharp_rows_within_the_p_rounding_bound(cuda_ok, causal, d):
+def test_sharp_rows(cuda_ok, causal, d):
     """Queries scaled by 10: nearly one-hot rows whose dominant weight is not
-    a power of two against the lazy reference, so its bf16 rounding (up to
-    2^-8 relative) is not averaged away.  Bound derived from the arithmetic:
-    1e-2 + 2^-8 |O_ref| (output rounding) + 2^-8 (|P| |V|)_ref (P rounding),
-    with (|P| |V|)_ref the oracle's attention over |V|."""
+    a power of two against the lazy reference.  O is normalised by the sum of
+    the bf16 weights the P V product used, so the dominant weight's own
+    rounding cancels: the storage bar holds with no allowance for the weights'
+    rounding."""
     case = W.attention(78 + d, 3, 4, 1024, 1024, d, causal, None)
     case.q = (case.q.float() * 10.0).to(torch.bfloat16)
     o, lse = run(case)
+    eo, el = check(o, lse, *oracle_of(case))
+    record(f"sharp rows q*10 d{d} causal={causal}", o_err=eo, lse_err=el)
+
+
+@pytest.mark.parametrize("bounded", [False, True])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_dominant_key_in_a_late_tile(cuda_ok, d, causal, bounded):
+    """Every query is beta times one key of a late key tile (beta in [1, 4]),
+    values of magnitude 4 to 6: rows are one-hot to within e^-8 .. e^-30, the
+    dominant weight is 2^k f against the reference the row's first tile set
+    (raised by whole binades when it would pass 2^16).  Plain bar everywhere;
+    and where the oracle's output equals the dominant key's value to 1e-4,
+    the GPU's output is that bf16 value exactly."""
+    B, H, N = 2, 3, 1024
+    case = W.attention_dominant_keys(300 + d + 2 * causal, B, H, N, d, causal)
+    q, k, v = case.q.cuda(), case.k.cuda(), case.v.cuda()
+    bound = None
+    if bounded:
+        bound = case.scale * float(case.q.float().norm(dim=-1).max()) * float(
+            case.k.float().norm(dim=-1).max())
+    o, lse = osm.attn_fwd(q, k, v, case.scale, causal, None, score_bound=bound)
+    assert osm.device_status() == 0
     ro, rl = oracle_of(case)
-    q64, k64, av = W.as_f64(case.q), W.as_f64(case.k), np.abs(W.as_f64(case.v))
-    pv, _ = oracle.attention_ref(q64, k64, av, case.scale, case.causal, None)
-    err = np.abs(W.as_f64(o) - ro)
-    assert float(np.max(err - 2.0 ** -8 * np.abs(ro) - 2.0 ** -8 * pv)) <= O_TOL
-    fin = np.isfinite(rl)
-    assert float(np.max(np.abs(W.as_f64(lse)[fin] - rl[fin]))) <= LSE_TOL
+    eo, el = check(o, lse, ro, rl)
+    record(f"dominant key d{d} causal={causal} bounded={bounded}", o_err=eo, lse_err=el)
+    vt = W.as_f64(case.v)[:, :, case.meta["target"], :]
+    onehot = np.all(np.abs(ro - vt) <= 1e-4, axis=-1)
+    assert onehot.mean() > 0.25
+    og = W.as_f64(o)
+    assert np.array_equal(og[onehot], vt[onehot])
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -201,41 +218,37 @@ def test_deterministic(cuda_ok):
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
-def _sample_rows(N, key_len, rng, n=96):
-    rows = set(rng.choice(N, size=n, replace=False).tolist())
-    rows |= {0, 1, 2, 127, 128, 255, 256, N - 1}
-    if key_len is not None:
-        rows |= {max(0, int(key_len) - 2), min(N - 1, int(key_len)), min(N - 1, int(key_len) + 1)}
-    return np.array(sorted(rows))
-
-
 def test_full_size_noncausal(cuda_ok):
-    """B4 H16 N4096 d128, non-causal: every row of 4 heads vs the oracle."""
+    """B4 H16 N4096 d128, non-causal: every row of 16 whole heads (four per
+    batch entry) against the oracle; the whole output finite."""
     case = W.attn()
     o, lse = run(case)
-    rng = np.random.default_rng(3)
-    for b, h in [(0, 0), (1, 7), (2, 15), (3, 3)]:
-        rows = _sample_rows(4096, None, rng, n=512)
-        (ro, rl), = oracle_of(case, rows=rows, bh=[(b, h)])
-        idx = torch.as_tensor(rows, device=o.device)
-        check(o[b:b + 1, h:h + 1, idx], lse[b:b + 1, h:h + 1, idx], ro, rl)
+    eo = el = 0.0
+    for b in range(4):
+        for h in (0, 5, 10, 15):
+            (ro, rl), = oracle_of(case, bh=[(b, h)])
+            e = check(o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1], ro, rl, plain=True)
+            eo, el = max(eo, e[0]), max(el, e[1])
+    record("attn B4 H16 N4096 d128 (16 whole heads)", o_err=eo, lse_err=el)
     assert torch.all(torch.isfinite(o)) and torch.all(torch.isfinite(lse))
 
 
 def test_full_size_causal_padded(cuda_ok):
-    """B8 H32 N8192 d128, causal, key_len ~ U[4096, 8192]: 8 heads including the
-    shortest and longest batch entries, sampled rows vs the oracle."""
+    """B8 H32 N8192 d128, causal, key_len ~ U[4096, 8192]: every row of 8 heads
+    -- the shortest and the longest batch entries and two more, heads 0 and
+    31 -- against the oracle; the whole output finite."""
     case = W.attn_causal()
     o, lse = run(case)
     kl = case.key_len.numpy()
-    bs = sorted({int(np.argmin(kl)), int(np.argmax(kl)), 0, 7})
-    rng = np.random.default_rng(4)
-    pairs = [(b, h) for b in bs for h in (0, 31)]
-    for b, h in pairs:
-        rows = _sample_rows(8192, kl[b], rng, n=160)
-        (ro, rl), = oracle_of(case, rows=rows, bh=[(b, h)])
-        idx = torch.as_tensor(rows, device=o.device)
-        check(o[b:b + 1, h:h + 1, idx], lse[b:b + 1, h:h + 1, idx], ro, rl)
+    bs = [int(np.argmin(kl)), int(np.argmax(kl))]
+    bs += [b for b in (0, 7, 1, 6) if b not in bs][:2]
+    eo = el = 0.0
+    for b in bs:
+        for h in (0, 31):
+            (ro, rl), = oracle_of(case, bh=[(b, h)])
+            e = check(o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1], ro, rl, plain=True)
+            eo, el = max(eo, e[0]), max(el, e[1])
+    record("attn causal+padding B8 H32 N8192 d128 (8 whole heads)", o_err=eo, lse_err=el)
     assert torch.all(torch.isfinite(o)) and torch.all(torch.isfinite(lse))
 
 

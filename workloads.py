@@ -137,6 +137,33 @@ def attention(seed: int, B: int, H: int, Nq: int, Nk: int, d: int, causal: bool,
     return AttnCase(q, k, v, 1.0 / math.sqrt(d), causal, kl, name=name)
 
 
+def attention_dominant_keys(seed: int, B: int, H: int, N: int, d: int, causal: bool,
+                            beta_range=(1.0, 4.0), v_range=(4.0, 6.0)) -> AttnCase:
+    """Nearly one-hot rows whose dominant key lies in a late key tile.
+
+    K is N(0,1).  Query row i is beta_i times one key t(i) (beta_i uniform on
+    ``beta_range``): t(i) = i when causal (the diagonal key, in the row's last
+    key tile), else a key of the last 128-key tile.  So s_i,t(i) ~ beta_i |k|^2
+    / sqrt(d) stands about beta_i * (sqrt(d) - 3) above the other scores.  V
+    entries have random signs and magnitudes uniform on ``v_range``.  Returns
+    the case and t as an int64 array [N].
+    """
+    k = to_bf16(normal_bhnd(seed, _K, B, H, N, d))
+    i = np.arange(N)
+    t = i.copy() if causal else (N - 1 - (i % min(N, 128)))
+    g = _gen(seed, _Q)
+    beta = g.uniform(*beta_range, size=(B, H, N, 1)).astype(np.float32)
+    q = to_bf16(k.float().numpy()[:, :, t, :] * beta)
+    gv = _gen(seed, _V)
+    mag = gv.uniform(*v_range, size=(B, H, N, d)).astype(np.float32)
+    sign = np.where(gv.random(size=(B, H, N, d)) < 0.5, -1.0, 1.0).astype(np.float32)
+    v = to_bf16(mag * sign)
+    case = AttnCase(q, k, v, 1.0 / math.sqrt(d), causal, None,
+                    name=f"dominant keys B{B} H{H} N{N} d{d} causal={causal}")
+    case.meta["target"] = t
+    return case
+
+
 def attn(seed: int = 3) -> AttnCase:
     return attention(seed, 4, 16, 4096, 4096, 128, False, None, "attn B4 H16 N4096 d128")
 
