@@ -37,13 +37,38 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "attn fwd TFLOPS & % BF16 tensor peak; softmax/decode GB/s & % HBM peak"
-ATTN_SRC = os.path.join(ROOT, "exact_tiled_attention_osm_gb300", "csrc", "attn_fwd.cu")
+CSRC = os.path.join(ROOT, "exact_tiled_attention_osm_gb300", "csrc")
 
-# DRAM traffic of one attention launch on this workload from an ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
-# source it was captured on (sha256 of attn_fwd.cu); None until captured.
-ATTN_TRAFFIC = {"bytes_per_launch": 1_330_000_000 + 519_670_000,
-                "source_sha256": "a5492fc1fa1c47ee81e318f62bd0e28ee5a0cc3951bb02647e222fb7ba5d4736"}
+# DRAM traffic of one launch on the bench workload from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum, summed over the kernels of the
+# operation), valid only for the kernel sources it was captured on (sha256 of
+# the listed files, concatenated); None until captured on the current source.
+KERNEL_TRAFFIC = {
+    # attn_fwd_kernel<false, 128>, causal+padding B8 H32 N8192: read 1,332,771,328
+    # + write 520,004,352
+    "attn_fwd_kernel": {"bytes_per_launch": 1_332_771_328 + 520_004_352,
+                        "sources": ["attn_fwd.cu", "ptx.cuh"],
+                        "source_sha256": "417ad53294c0efbf94bd80c8f6872e948e050c6d9ec98e55496dff4eb6f2854a"},
+    # softmax_rows_cluster<8>, 4096 x 32768: read 536,905,216 + write 483,361,536
+    "softmax_rows": {"bytes_per_launch": 536_905_216 + 483_361_536,
+                     "sources": ['softmax_rows.cu', 'exp_le0.cuh', 'ptx.cuh'],
+                     "source_sha256": "04b2b74e40e3199b82f751e4a512ae8f3a306df9f5f59e3295a67a3b36aeb1e3"},
+    # decode_split_kernel read 17,360,807,936 + write 11,566,848;
+    # merge_kernel read 17,051,648 + write 0
+    "decode_splitkv": {"bytes_per_launch": 17_360_807_936 + 11_566_848 + 17_051_648,
+                       "sources": ['decode.cu', 'ptx.cuh'],
+                       "source_sha256": "2b14b3572fac049d7522e60cafb613da511765ee36992c23d4a268644360114f"},
+}
+
+
+def captured_traffic(kernel):
+    t = KERNEL_TRAFFIC[kernel]
+    h = hashlib.sha256()
+    for name in t["sources"]:
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(f.read())
+    return t["bytes_per_launch"] if h.hexdigest() == t["source_sha256"] else None
+
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -55,11 +80,6 @@ def peaks():
             d = json.load(f)
         return d, "measured"
     return dict(FALLBACK_PEAKS), "fallback"
-
-
-def sha256(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
 
 
 # ----------------------------------------------------------------- algorithmic work
@@ -373,7 +393,8 @@ def reduce_max(times: dict, world: int, device) -> dict:
 def profile_case(spec: str, iters: int):
     """Run one operation `iters` times on a given shape (for ncu captures).
 
-    spec: "attn:B,H,N[,causal][,d64]" | "attnqk:B,H,N[,causal]" (QK-norm inputs with
+    spec: "attn:B,H,N[,causal][,d64]" | "attnnorm:B,H,N[,causal][,d64]" (the normalised
+          form) | "attnqk:B,H,N[,causal]" (QK-norm inputs with
           their score bound) | "bwd:B,H,N[,causal][,d64]" | "softmax:rows,cols"
           | "topk:rows,cols,k"
           | "decode:B,H,Nk[,splits]"
@@ -385,14 +406,16 @@ def profile_case(spec: str, iters: int):
     op, _, arg = spec.partition(":")
     parts = arg.split(",")
     dev = torch.device("cuda", 0)
-    if op == "attn":
+    if op in ("attn", "attnnorm"):
+        # attnnorm: the normalised form (one division per key tile)
         B, H, N = (int(x) for x in parts[:3])
         causal = "causal" in parts[3:]
         hd = 64 if "d64" in parts[3:] else 128
         c = W.attention(4, B, H, N, N, hd, causal, (N // 2, N) if causal else None)
         q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
         kl = c.key_len.to(dev) if c.key_len is not None else None
-        run = lambda: osm.attn_fwd(q, k, v, c.scale, causal, kl)
+        norm = op == "attnnorm"
+        run = lambda: osm.attn_fwd(q, k, v, c.scale, causal, kl, normalised=norm)
         work = attn_flops(B, H, N, N, hd, causal, None if kl is None else c.key_len.numpy())
         unit = "TFLOP/s"
     elif op == "attnqk":
@@ -568,9 +591,7 @@ def main():
     soft_gbs = world * res["softmax_bytes"] / (mx["soft_ms"] * 1e-3) / 1e9
     dec_gbs = world * res["decode_bytes"] / (mx["dec_ms"] * 1e-3) / 1e9
     per_gpu_tf = attn_tf / world
-    src_sha = sha256(ATTN_SRC)
-    traffic = (ATTN_TRAFFIC["bytes_per_launch"]
-               if ATTN_TRAFFIC["source_sha256"] == src_sha else None)
+    traffic = captured_traffic("attn_fwd_kernel")
     peak_tc = pk["bf16_tflops"]
     roofline = {"bound": "tensor", "achieved": per_gpu_tf, "peak": peak_tc, "unit": "TFLOP/s",
                 "frac": per_gpu_tf / peak_tc, "traffic": traffic,
@@ -583,12 +604,13 @@ def main():
         "softmax_rows": {"value": soft_gbs, "unit": "GB/s", "ms": mx["soft_ms"],
                          "roofline": {"bound": "hbm", "achieved": soft_gbs / world, "peak": hbm,
                                       "unit": "GB/s", "frac": soft_gbs / world / hbm,
-                                      "traffic": None, "per_launch_bytes": res["softmax_bytes"],
+                                      "traffic": captured_traffic("softmax_rows"),
+                                      "per_launch_bytes": res["softmax_bytes"],
                                       "peak_kind": f"{pk_kind} copy"}},
         "decode_splitkv": {"value": dec_gbs, "unit": "GB/s", "ms": mx["dec_ms"],
                            "roofline": {"bound": "hbm", "achieved": dec_gbs / world, "peak": hbm,
                                         "unit": "GB/s", "frac": dec_gbs / world / hbm,
-                                        "traffic": None,
+                                        "traffic": captured_traffic("decode_splitkv"),
                                         "per_launch_bytes": res["decode_bytes"],
                                         "peak_kind": f"{pk_kind} copy",
                                         "note": "split kernel + merge kernel, one pass"}},

@@ -39,7 +39,8 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libosm.so")
 
-OSM_OK, OSM_ERR_INVALID_VALUE, OSM_ERR_UNSUPPORTED, OSM_ERR_CUDA, OSM_ERR_TIMEOUT = range(5)
+(OSM_OK, OSM_ERR_INVALID_VALUE, OSM_ERR_UNSUPPORTED, OSM_ERR_CUDA, OSM_ERR_TIMEOUT,
+ OSM_ERR_CONFLICT) = range(6)
 OSM_F32, OSM_BF16 = 0, 1
 
 # exported names and their C signatures (include/osm.h)
@@ -49,6 +50,7 @@ SIGNATURES = {
     "osm_softmax_topk": (_I, [_P, _I64, _I64, _I, _P, _P, _P]),
     "osm_attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P]),
     "osm_attn_fwd_bounded": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _F, _P]),
+    "osm_attn_fwd_normalised": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P]),
     "osm_attn_bwd_workspace_bytes": (_SZ, [_I, _I, _I]),
     "osm_attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P,
                           _SZ, _P]),
@@ -159,12 +161,16 @@ def softmax_topk(x, k, idx=None, prob=None):
 
 
 def attn_fwd(q, k, v, scale=None, causal=False, key_len=None, out=None, lse=None,
-             score_bound=None):
+             score_bound=None, normalised=False):
     """Attention forward.  q [B,H,Nq,d], k, v [B,H,Nk,d] bf16 CUDA; key_len int32 [B] or None.
 
     Returns (o [B,H,Nq,d] bf16, lse [B,H,Nq] fp32).  `score_bound`: a known
     upper bound on the scaled scores (osm_attn_fwd_bounded); None = unknown.
+    `normalised`: compute the normalised form, dividing by l after every key
+    tile (osm_attn_fwd_normalised; not with a score bound).
     """
+    if normalised and score_bound is not None:
+        raise ValueError("normalised form takes no score bound")
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, torch.bfloat16, q.device)
     if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
@@ -185,7 +191,12 @@ def attn_fwd(q, k, v, scale=None, causal=False, key_len=None, out=None, lse=None
         kl = key_len.data_ptr()
     lib = load_library()
     with torch.cuda.device(q.device):
-        if score_bound is None:
+        if normalised:
+            _check(lib.osm_attn_fwd_normalised(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                               o.data_ptr(), lse_t.data_ptr(), B, H, Nq, Nk, d,
+                                               float(scale), int(bool(causal)), kl, _stream(q)),
+                   "osm_attn_fwd_normalised")
+        elif score_bound is None:
             _check(lib.osm_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                     lse_t.data_ptr(), B, H, Nq, Nk, d, float(scale),
                                     int(bool(causal)), kl, _stream(q)), "osm_attn_fwd")
@@ -428,6 +439,6 @@ def device_status(device=None) -> int:
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     with torch.cuda.device(dev):
         st = lib.osm_device_status(torch.cuda.current_stream(dev).cuda_stream, ctypes.byref(w))
-    if st not in (OSM_OK, OSM_ERR_TIMEOUT):
+    if st not in (OSM_OK, OSM_ERR_TIMEOUT, OSM_ERR_CONFLICT):
         raise OsmError(st, "osm_device_status")
     return int(w.value)

@@ -21,7 +21,7 @@ inline osm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? OSM_OK : 
 
 extern "C" {
 
-int osm_abi_version(void) { return 101; }
+int osm_abi_version(void) { return 102; }
 
 const char* osm_status_string(osm_status st) {
   switch (st) {
@@ -30,6 +30,8 @@ const char* osm_status_string(osm_status st) {
     case OSM_ERR_UNSUPPORTED: return "OSM_ERR_UNSUPPORTED: case not implemented by this build";
     case OSM_ERR_CUDA: return "OSM_ERR_CUDA: CUDA launch or runtime error";
     case OSM_ERR_TIMEOUT: return "OSM_ERR_TIMEOUT: a bounded device-side wait ran out";
+    case OSM_ERR_CONFLICT:
+      return "OSM_ERR_CONFLICT: two forward launches in flight shared a work-item counter";
   }
   return "unknown osm_status";
 }
@@ -67,7 +69,8 @@ constexpr int kMaxSeq = 1 << 30;
 
 osm_status attn_fwd_checked(const void* q, const void* k, const void* v, void* o, float* lse,
                             int B, int H, int Nq, int Nk, int d, float scale, int causal,
-                            const int32_t* key_len, float score_bound, osm_stream_t stream) {
+                            const int32_t* key_len, float score_bound, bool normalised,
+                            osm_stream_t stream) {
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return OSM_ERR_INVALID_VALUE;
   if (causal != 0 && causal != 1) return OSM_ERR_INVALID_VALUE;
   if (!(scale > 0.f) || !std::isfinite(scale)) return OSM_ERR_INVALID_VALUE;
@@ -81,8 +84,8 @@ osm_status attn_fwd_checked(const void* q, const void* k, const void* v, void* o
   if (static_cast<int64_t>(B) * H > 0x7fffffffLL) return OSM_ERR_UNSUPPORTED;
   bool tmap_ok = true;
   cudaError_t e = osm::launch_attn_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, key_len,
-                                       score_bound, reinterpret_cast<cudaStream_t>(stream),
-                                       &tmap_ok);
+                                       score_bound, normalised,
+                                       reinterpret_cast<cudaStream_t>(stream), &tmap_ok);
   if (!tmap_ok) return OSM_ERR_UNSUPPORTED;  // shape the TMA descriptor cannot express
   return from_cuda(e);
 }
@@ -92,7 +95,14 @@ osm_status osm_attn_fwd(const void* q, const void* k, const void* v, void* o, fl
                         int H, int Nq, int Nk, int d, float scale, int causal,
                         const int32_t* key_len, osm_stream_t stream) {
   return attn_fwd_checked(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, key_len,
-                          std::numeric_limits<float>::quiet_NaN(), stream);
+                          std::numeric_limits<float>::quiet_NaN(), false, stream);
+}
+
+osm_status osm_attn_fwd_normalised(const void* q, const void* k, const void* v, void* o,
+                                   float* lse, int B, int H, int Nq, int Nk, int d, float scale,
+                                   int causal, const int32_t* key_len, osm_stream_t stream) {
+  return attn_fwd_checked(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, key_len,
+                          std::numeric_limits<float>::quiet_NaN(), true, stream);
 }
 
 osm_status osm_attn_fwd_bounded(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -100,7 +110,7 @@ osm_status osm_attn_fwd_bounded(const void* q, const void* k, const void* v, voi
                                 const int32_t* key_len, float score_bound, osm_stream_t stream) {
   if (!std::isfinite(score_bound) || std::fabs(score_bound) > 1e30f) return OSM_ERR_INVALID_VALUE;
   return attn_fwd_checked(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, key_len, score_bound,
-                          stream);
+                          false, stream);
 }
 
 size_t osm_attn_bwd_workspace_bytes(int B, int H, int Nq) {
@@ -253,7 +263,8 @@ osm_status osm_device_status(osm_stream_t stream, uint32_t* word) {
   e = osm::read_and_clear_bwd_error(&wb);
   if (e != cudaSuccess) return OSM_ERR_CUDA;
   if (*word == 0) *word = wb;
-  return *word ? OSM_ERR_TIMEOUT : OSM_OK;
+  if (*word == 0) return OSM_OK;
+  return (*word >> 24) == 0x0Cu ? OSM_ERR_CONFLICT : OSM_ERR_TIMEOUT;
 }
 
 }  // extern "C"

@@ -185,7 +185,10 @@ struct Params {
   __nv_bfloat16* o;
   float* lse;
   unsigned int* err;
-  unsigned int* next_item;  // work-item counter, zero at launch
+  // work-item counter: the launch's tag in the low 32 bits, the count of
+  // items handed out in the high 32 bits (zero at launch)
+  unsigned long long* next_item;
+  unsigned int tag;
 };
 
 struct Item {
@@ -213,18 +216,28 @@ __device__ __forceinline__ Item item_info(const Params& p, int item) {
 
 __device__ unsigned int g_err_word;
 // Work-item counters.  Each launch takes the next entry (round robin) and
-// zeroes it on its own stream first, so launches on different streams only
-// share a counter when more than kCounters of them are in flight at once.
-// Launches captured into a CUDA graph keep their entry for every replay, so
-// they draw from a second range that direct launches never use.
+// resets it on its own stream first to (count 0, its own tag), so launches on
+// different streams only share a counter when more than kCounters of them are
+// in flight at once -- and then the older one finds a foreign tag when it
+// next draws an item, records kConflictSite and stops drawing: its output is
+// wrong, but osm_device_status reports it.  Launches captured into a CUDA
+// graph keep their entry (and tag) for every replay, so they draw from a
+// second range that direct launches never use.
 constexpr int kCounters = 1024;
-__device__ unsigned int g_item_counter[2 * kCounters];
+__device__ unsigned long long g_item_counter[2 * kCounters];
+constexpr unsigned kConflictSite = 0x0C000001u;
 
 // kBounded: every row starts from the caller's bound (p.m_init finite), so no
 // tile looks for the maximum and an all-underflow start can lower the reference.
 // D: the head dimension, 64 or 128 (a 64-column tile uses half of each slot and
 // half of each O~ region; the softmax is the same).
-template <bool kBounded, int D>
+// kNorm: the normalised form of the recurrence ("Online softmax",
+// zerotofrontier.app, "From weights to outputs", the second way to write it):
+// the output accumulator holds o = O~ / l after every key step.  Each tile's P
+// is divided by the new l and the accumulator scaled by l_old / l_new before
+// the P V product adds to it; the epilogue divides nothing.  Built to measure
+// what the per-step division costs against the single division at the end.
+template <bool kBounded, int D, bool kNorm = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -304,6 +317,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         iq_advance();
         return true;
       };
+      // Take a ticket: the counter's count, if its tag is this launch's; a
+      // foreign tag ends this CTA's items (see g_item_counter).
+      auto draw = [&]() -> unsigned int {
+        const unsigned long long old = atomicAdd(p.next_item, 1ull << 32);
+        if (static_cast<unsigned int>(old) != p.tag) {
+          atomicCAS(p.err, 0u, kConflictSite);
+          return 0x7fffffffu;
+        }
+        return static_cast<unsigned int>(old >> 32);
+      };
       // the first item of every CTA is its own index (grid <= items); the
       // rest come from the counter, one item ahead of the one being loaded
       int item = blockIdx.x;
@@ -339,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           q_fill = loaded & 1;
           ++loaded;
           // the counter's reply is first needed after this item's first K/V copies
-          ticket = atomicAdd(p.next_item, 1u);
+          ticket = draw();
           // pair e of the item: K_e (e < n) and V_{e-1} (e > 0), one barrier
           for (int e = 0; ok && e <= it.n_kv; ++e) {
             if (!(ok = wait_one(bar(KV_EMPTY + slot), ph ^ 1, kSite | 2))) break;
@@ -363,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok && !published) ok = publish_next();
           }
         } else {
-          ticket = atomicAdd(p.next_item, 1u);
+          ticket = draw();
         }
         if (ok && !published) ok = publish_next();
       }
@@ -550,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             m_ref = m_new;
             resc = true;
           }
-          if (__any_sync(0xffffffffu, resc)) {
+          if (!kNorm && __any_sync(0xffffffffu, resc)) {  // o = O~ / l needs no rescale
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
               uint32_t orr[32];
@@ -565,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // pass over kNch chunks of kCw columns (S read from TMEM), each chunk
         // two-phase: all scale/subtracts, then kCw independent exp2, then the
         // sums and bf16 packs -- so the MUFU latency is covered
-        constexpr int kCw = (D == 64 || kBounded) ? 64 : 32;
+        constexpr int kCw = ((D == 64 && !kNorm) || kBounded) ? 64 : 32;
         constexpr int kNch = kKeys / kCw;
         float la[4] = {0.f, 0.f, 0.f, 0.f};
         // a chunk whose sum passes thr moves the reference (see below)
@@ -667,14 +690,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_st();
               }
               // O~'s last update (P V of the previous tile) completed before S
-              // (before a row's first P V it holds no value: scaling it is harmless)
+              // (before a row's first P V it holds no value: scaling it is
+              // harmless); o = O~ / l is not scaled
+              if constexpr (!kNorm) {
 #pragma unroll 1
-              for (int c = 0; c < D / 32; ++c) {
-                uint32_t orr[32];
-                tmem_ld_x32(tO + 32 * c, orr);
+                for (int c = 0; c < D / 32; ++c) {
+                  uint32_t orr[32];
+                  tmem_ld_x32(tO + 32 * c, orr);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-                tmem_st_x32(tO + 32 * c, orr);
+                  for (int e = 0; e < 32; ++e)
+                    orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                  tmem_st_x32(tO + 32 * c, orr);
+                }
               }
               exp_chunk();
               csum = (cs[0] + cs[1]) + (cs[2] + cs[3]);
@@ -696,6 +723,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st_cols_nowait(tS + (kCw / 2) * ch, pk);
         }
         tmem_wait_st();
+        if constexpr (kNorm) {
+          // o_new = (l_old o + P V) / l_new: P times 1 / l_new (the stored bf16
+          // pairs, rounded again), o times l_old / l_new.  The previous P V has
+          // completed (it was issued before this tile's S).
+          const float l_new = l + ((la[0] + la[1]) + (la[2] + la[3]));
+          const float inv = l_new > 0.f ? 1.f / l_new : 0.f;
+          const float fo = l * inv;
+#pragma unroll 1
+          for (int c = 0; c < kKeys / 64; ++c) {
+            uint32_t pp[32];
+            tmem_ld_x32(tS + 32 * c, pp);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(pp[e] << 16) * inv,
+                                                        __uint_as_float(pp[e] & 0xffff0000u) * inv);
+              pp[e] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            tmem_st_x32(tS + 32 * c, pp);
+          }
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t orr[32];
+            tmem_ld_x32(tO + 32 * c, orr);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * fo);
+            tmem_st_x32(tO + 32 * c, orr);
+          }
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
@@ -708,7 +763,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       of_ph ^= 1;
       tc_fence_after();
-      const float inv = l + corr > 0.f ? 1.f / (l + corr) : 0.f;
+      const float inv = kNorm ? (l > 0.f ? 1.f : 0.f) : (l + corr > 0.f ? 1.f / (l + corr) : 0.f);
       // O = O~ / l in bf16, a 32-column chunk at a time: each thread puts its
       // row's 64 bytes into the warp's staging area, then the warp stores 8
       // rows x 64 contiguous bytes per instruction (4 lanes per row segment)
@@ -785,8 +840,8 @@ int sm_count_current_device() {
 
 cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                             int B, int H, int Nq, int Nk, int d, float scale, int causal,
-                            const int32_t* key_len, float score_bound, cudaStream_t s,
-                            bool* tmap_ok) {
+                            const int32_t* key_len, float score_bound, bool normalised,
+                            cudaStream_t s, bool* tmap_ok) {
   using namespace attn;
   *tmap_ok = true;
   const int64_t rows = static_cast<int64_t>(B) * H * Nq;
@@ -833,33 +888,46 @@ cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   e = cudaStreamIsCapturing(s, &cap);
   if (e != cudaSuccess) return e;
-  const unsigned int slot = cap == cudaStreamCaptureStatusNone
-                                ? next_direct.fetch_add(1) % kCounters
-                                : kCounters + next_captured.fetch_add(1) % kCounters;
-  p.next_item = static_cast<unsigned int*>(ctrp) + slot;
-  e = cudaMemsetAsync(p.next_item, 0, sizeof(unsigned int), s);
+  const unsigned int seq =
+      cap == cudaStreamCaptureStatusNone ? next_direct.fetch_add(1) : next_captured.fetch_add(1);
+  const unsigned int slot = (cap == cudaStreamCaptureStatusNone ? 0 : kCounters) + seq % kCounters;
+  p.next_item = static_cast<unsigned long long*>(ctrp) + slot;
+  p.tag = seq;
+  // reset: tag in the low word, count 0 in the high word
+  auto memset32 = memset_d32_fn();
+  if (!memset32) return cudaErrorNotSupported;
+  if (memset32(reinterpret_cast<CUdeviceptr>(p.next_item), p.tag, 1, s) != CUDA_SUCCESS)
+    return cudaErrorUnknown;
+  e = cudaMemsetAsync(reinterpret_cast<unsigned int*>(p.next_item) + 1, 0, sizeof(unsigned int), s);
   if (e != cudaSuccess) return e;
   // the shared-memory opt-in is per function and per device
-  static unsigned long long attr_done = 0;
+  static std::atomic<unsigned long long> attr_done{0};
   int dev = 0;
   e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
-  if (!(attr_done & bit)) {
+  if (!(attr_done.load() & bit)) {
     for (const void* fn : {reinterpret_cast<const void*>(attn_fwd_kernel<false, 128>),
                            reinterpret_cast<const void*>(attn_fwd_kernel<true, 128>),
                            reinterpret_cast<const void*>(attn_fwd_kernel<false, 64>),
-                           reinterpret_cast<const void*>(attn_fwd_kernel<true, 64>)}) {
+                           reinterpret_cast<const void*>(attn_fwd_kernel<true, 64>),
+                           reinterpret_cast<const void*>(attn_fwd_kernel<false, 128, true>),
+                           reinterpret_cast<const void*>(attn_fwd_kernel<false, 64, true>)}) {
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(kSmemBytes));
       if (e != cudaSuccess) return e;
     }
-    attr_done |= bit;
+    attr_done.fetch_or(bit);
   }
   const int grid = static_cast<int>(items < sm_count_current_device() ? items
                                                                       : sm_count_current_device());
   const bool bounded = std::isfinite(score_bound);
-  if (d == 128) {
+  if (normalised) {
+    if (d == 128)
+      attn_fwd_kernel<false, 128, true><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+    else
+      attn_fwd_kernel<false, 64, true><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+  } else if (d == 128) {
     if (bounded)
       attn_fwd_kernel<true, 128><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
     else

@@ -21,8 +21,8 @@ cudaError_t launch_softmax_topk(const float* x, int64_t rows, int64_t cols, int 
 // attn_fwd.cu
 cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                             int B, int H, int Nq, int Nk, int d, float scale, int causal,
-                            const int32_t* key_len, float score_bound, cudaStream_t s,
-                            bool* tmap_ok);
+                            const int32_t* key_len, float score_bound, bool normalised,
+                            cudaStream_t s, bool* tmap_ok);
 cudaError_t read_and_clear_device_error(cudaStream_t s, uint32_t* word);
 cudaError_t launch_bounded_wait_selftest(cudaStream_t s);
 

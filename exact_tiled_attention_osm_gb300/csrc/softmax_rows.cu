@@ -19,15 +19,13 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "exp_le0.cuh"
 #include "ptx.cuh"
 
 namespace osm {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-// log2(e) split into an fp32 head and its remainder, for argument reduction.
-constexpr float kLog2eHi = 1.44269502162933349609375f;
-constexpr float kLog2eLo = 1.925963033500011079e-8f;
 constexpr float kNegInf = -__builtin_huge_valf();
 
 // weight of a summary with max m when brought to the common max mn (mn >= m);
@@ -41,19 +39,6 @@ __device__ __forceinline__ void merge_ml(float& m, float& l, float mo, float lo)
   const float mn = fmaxf(m, mo);
   l = l * rebase(m, mn) + lo * rebase(mo, mn);
   m = mn;
-}
-
-// exp(d) for d <= 0, with the base-2 argument d*log2(e) split into an integer
-// n and a remainder f (Cody & Waite range reduction) so the remainder keeps
-// full precision; results below the normal fp32 range flush to 0.
-__device__ __forceinline__ float exp_le0(float d) {
-  d = fmaxf(d, -100.f);  // also maps -inf (and -inf - -inf) to a flushed 0
-  const float n = rintf(d * kLog2eHi);
-  float f = fmaf(d, kLog2eHi, -n);
-  f = fmaf(d, kLog2eLo, f);
-  const float r = ptx::ex2(f);
-  const int ni = static_cast<int>(n);
-  return ni < -125 ? 0.f : r * __int_as_float((ni + 127) << 23);
 }
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

@@ -30,6 +30,7 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "exp_le0.cuh"
 #include "ptx.cuh"
 
 namespace osm {
@@ -38,27 +39,12 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr float kLog2e = 1.4426950408889634f;
-// log2(e) split into an fp32 head and its remainder, for argument reduction
-constexpr float kLog2eHi = 1.44269502162933349609375f;
-constexpr float kLog2eLo = 1.925963033500011079e-8f;
 constexpr float kNegInf = -__builtin_huge_valf();
 constexpr int kNoIndex = 0x7fffffff;  // empty list slot: after every real entry
 
 // the total order of (value, index) pairs
 __device__ __forceinline__ bool before(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
-}
-
-// exp(d) for d <= 0 (Cody & Waite split of d*log2(e) into an integer and a
-// remainder, so the remainder keeps full precision); flushes below 2^-125
-__device__ __forceinline__ float exp_le0(float d) {
-  d = fmaxf(d, -100.f);
-  const float n = rintf(d * kLog2eHi);
-  float f = fmaf(d, kLog2eHi, -n);
-  f = fmaf(d, kLog2eLo, f);
-  const float r = ptx::ex2(f);
-  const int ni = static_cast<int>(n);
-  return ni < -125 ? 0.f : r * __int_as_float((ni + 127) << 23);
 }
 
 // K best (value, index) pairs seen so far, sorted by the order above

@@ -1,5 +1,5 @@
-// tmap.h — host-side TMA descriptor encoding through the driver entry point
-// (no link against libcuda; the entry point is fetched from the runtime).
+// tmap.h — host-side driver calls reached through the runtime's entry-point
+// lookup (no link against libcuda): TMA descriptor encoding and a 32-bit fill.
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -8,17 +8,29 @@
 namespace osm {
 
 inline PFN_cuTensorMapEncodeTiled_v12000 tmap_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {  // looked up once, thread-safe
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
+  return fn;
+}
+
+// cuMemsetD32Async (32-bit fill on a stream), fetched the same way
+using MemsetD32Fn = CUresult (*)(CUdeviceptr, unsigned int, size_t, CUstream);
+inline MemsetD32Fn memset_d32_fn() {
+  static MemsetD32Fn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuMemsetD32Async", &p, 3020, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<MemsetD32Fn>(p);
+    return static_cast<MemsetD32Fn>(nullptr);
+  }();
   return fn;
 }
 

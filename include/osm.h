@@ -46,7 +46,9 @@ typedef enum {
   OSM_ERR_INVALID_VALUE = 1, /* null pointer, bad size, misalignment, small workspace */
   OSM_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement (e.g. d) */
   OSM_ERR_CUDA = 3,          /* a CUDA launch or runtime call failed */
-  OSM_ERR_TIMEOUT = 4        /* a bounded device-side wait ran out (osm_device_status) */
+  OSM_ERR_TIMEOUT = 4,       /* a bounded device-side wait ran out (osm_device_status) */
+  OSM_ERR_CONFLICT = 5       /* two forward launches in flight shared a work-item
+                                counter (osm_device_status; see osm_attn_fwd) */
 } osm_status;
 
 typedef enum { OSM_F32 = 0, OSM_BF16 = 1 } osm_dtype;
@@ -117,9 +119,17 @@ osm_status osm_softmax_topk(const float *x, int64_t rows, int64_t cols, int k, i
  * moves it only when a term would exceed 2^16 or all terms so far underflow.
  * No score matrix is written to memory.
  * Work is handed to the thread blocks through a library-owned counter that
- * the call zeroes on `stream` (a 4-byte memset, then the kernel); calls on
- * different streams may overlap as long as fewer than 1024 direct calls (and,
- * separately, 1024 captured-graph launches) are in flight at once.
+ * the call resets on `stream` (two 4-byte fills, then the kernel): count 0
+ * and the launch's own tag.  Calls on different streams may overlap as long
+ * as fewer than 1024 direct calls (and, separately, 1024 captured-graph
+ * launches) are in flight at once.  If more are, a launch whose counter was
+ * reset by a later one finds a foreign tag when it next draws work, stops
+ * drawing and records OSM_ERR_CONFLICT for osm_device_status: its outputs are
+ * then wrong (and so may the later launch's be), but not silently.  A launch
+ * captured into a CUDA graph keeps its counter and tag for every replay, so
+ * two instantiations of one captured forward (or two replays of one graph on
+ * different streams) must not run at the same time: they share a counter
+ * without the tag telling them apart.
  *
  *   q     [B, H, Nq, d] bf16;  k, v [B, H, Nk, d] bf16 (read only).
  *   o     [B, H, Nq, d] bf16 (written);  lse [B, H, Nq] fp32 (written).
@@ -146,12 +156,16 @@ osm_status osm_attn_fwd(const void *q, const void *k, const void *v, void *o, fl
  * example queries and keys normalised by QK-norm, so |s| <= scale |q| |k|) it
  * can be subtracted once and the running maximum is never needed.  Every row
  * starts from `score_bound` (scaled-score units, natural log) instead of 0.
- * With a valid bound no rescale happens unless the bound lies more than
- * about 87 (2^126 in weight) above a row's maximum, where all terms would
- * underflow; the kernel then lowers the reference (the pages' warning that a
- * loose bound risks underflowing every term).  A score above the bound by
- * more than 16 binades' worth raises it.  Either way the result is exact;
- * the bound only decides how often a chunk is redone.
+ * With a valid bound the reference moves only in three cases: when every
+ * term so far would underflow (the bound lies more than about 87, 2^126 in
+ * weight, above a row's scores: the pages' warning that a loose bound risks
+ * underflowing every term), the kernel lowers it; a score above the bound by
+ * more than 16 binades' worth raises it; and a chunk of keys after the first
+ * tile that outweighs everything before it in the row moves it to that
+ * chunk's maximum (lowering it by at most 120 binades), so that a dominant
+ * term has weight exactly 1.  The first tile's terms, taken against the bound,
+ * enter the divisor as rounded to bf16.  Either way the result is exact to
+ * rounding; the bound only decides how often a chunk is redone.
  *
  * Arguments as osm_attn_fwd, plus:
  *   score_bound  finite, |score_bound| <= 1e30 (else OSM_ERR_INVALID_VALUE).
@@ -160,6 +174,27 @@ osm_status osm_attn_fwd_bounded(const void *q, const void *k, const void *v, voi
                                 float *lse, int B, int H, int Nq, int Nk, int d, float scale,
                                 int causal, const int32_t *key_len, float score_bound,
                                 osm_stream_t stream);
+
+/*
+ * osm_attn_fwd_normalised — osm_attn_fwd computed in the normalised form.
+ *
+ * [P3] "From weights to outputs" writes the same recurrence a second way, the
+ * form of the original FlashAttention: keep the output normalised after every
+ * key block, o_new = (l_old e^{m_old - m_new} o + sum_j e^{s_j - m_new} v_j)
+ * / l_new, one division per block instead of one at the end, and calls the
+ * per-block division wasted work.  This entry point computes that form (the
+ * tile's weights are divided by the new l before the P V product and the
+ * accumulator is scaled by l_old / l_new) so that its cost can be measured
+ * against osm_attn_fwd.  Results agree with osm_attn_fwd to rounding; the
+ * weights are rounded to bf16 twice (as e^{s - m}, then divided by l), so a
+ * row concentrated on a few keys is off by up to twice the bf16 unit
+ * roundoff of its weights.
+ *
+ * Arguments, layouts and errors as osm_attn_fwd.
+ */
+osm_status osm_attn_fwd_normalised(const void *q, const void *k, const void *v, void *o,
+                                   float *lse, int B, int H, int Nq, int Nk, int d, float scale,
+                                   int causal, const int32_t *key_len, osm_stream_t stream);
 
 /*
  * osm_attn_bwd — gradients of exact softmax attention, BF16 in and out.
@@ -345,9 +380,11 @@ const char *osm_status_string(osm_status status);
 /*
  * osm_device_status — synchronise `stream`, then read and clear the current
  * device's error word that bounded waits write.  *word = 0 means no device
- * wait ran out since the last call; otherwise it identifies the wait site and
- * the return value is OSM_ERR_TIMEOUT.  Returns OSM_ERR_CUDA if the
- * synchronisation itself fails.  Not a hot-path call.
+ * wait ran out since the last call; otherwise it identifies the site: a
+ * word whose top byte is 0x0C is a shared work-item counter (return value
+ * OSM_ERR_CONFLICT), any other a bounded wait that ran out (OSM_ERR_TIMEOUT).
+ * Returns OSM_ERR_CUDA if the synchronisation itself fails.  Not a hot-path
+ * call.
  */
 osm_status osm_device_status(osm_stream_t stream, uint32_t *word);
 

@@ -47,11 +47,11 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    for st in range(5):
+    for st in range(6):
         s = osm.status_string(st)
         assert s.startswith("OSM_")
     assert "unknown" in osm.status_string(99)
-    assert lib.osm_abi_version() == 101
+    assert lib.osm_abi_version() == 102
 
 
 def test_workspace_bytes_formula(lib):
@@ -90,8 +90,9 @@ def test_softmax_topk_validation(lib):
     assert f(None, 0, 100, 8, None, None, None) == osm.OSM_OK                   # empty: no-op
 
 
-def test_attn_validation(lib):
-    f = lib.osm_attn_fwd
+@pytest.mark.parametrize("entry", ["osm_attn_fwd", "osm_attn_fwd_normalised"])
+def test_attn_validation(lib, entry):
+    f = getattr(lib, entry)
     ok_args = [FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 128, 128, 0.088, 0, None, None]
 
     def call(**kw):

@@ -21,7 +21,7 @@ from bars import check_attention, record
 pytestmark = pytest.mark.gpu
 
 
-def check(o, lse, ro, rl):
+def check(o, lse, ro, rl, plain=False):
     return check_attention(W.as_f64(o), W.as_f64(lse), ro, rl, plain)
 
 

@@ -25,7 +25,7 @@ def ref_decode(q, k, v, scale, key_len):
                                 None if key_len is None else key_len.cpu().numpy())
 
 
-def check_bf16(o, lse, ro, rl):
+def check_bf16(o, lse, ro, rl, plain=False):
     return check_attention(W.as_f64(o)[:, :, 0], W.as_f64(lse), ro[:, :, 0], rl[:, :, 0], plain)
 
 
