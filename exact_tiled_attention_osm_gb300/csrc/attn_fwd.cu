@@ -21,14 +21,18 @@
 //              V_{j-1} (the two tiles step j reads) into one of two pairs of
 //              shared-memory slots (128-byte swizzle) under one mbarrier, so
 //              each key step costs the MMA thread one wait and one release.
-//   warp 1     MMA issuer (one thread): per key step j and query tile t,
+//   warp 1     MMA issuer: per key step j and query tile t,
 //              O~_t += P_t V_{j-1} (P_t read straight from TMEM), then
 //              S_t = Q_t K_j^T into TMEM over the columns P_t occupied (the
-//              tensor pipe runs them in issue order).
+//              tensor pipe runs them in issue order).  The whole warp runs
+//              the loop and one elected lane issues each MMA: the descriptor
+//              arithmetic then stays warp-uniform, which keeps the issue rate
+//              above the tensor pipe's even with two softmax warps competing
+//              for the same sub-partition (a single-lane issuer fell below it).
 //   warps 4-7  softmax for query tile 0; warps 8-11 for tile 1.  One thread
-//              per query row, a rolled loop over the tile's columns in chunks
-//              (32 wide at d = 128, 64 wide at d = 64 and with a caller's
-//              bound: measured best for each; no register spills): the chunk
+//              per query row, a rolled loop over the tile's columns in
+//              64-column chunks (32 in the normalised form, for registers; no
+//              register spills): the chunk
 //              TMEM -> registers, mask, scale and subtract the reference in
 //              packed f32x2, independent exp2 (so the MUFU latency is
 //              covered), row sum, bf16 pack, store P over the S columns
@@ -119,52 +123,13 @@ constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);  // Q, K both K-ma
 constexpr unsigned kSite = 0x01000000u;
 
 
-// Eight K-steps of one product from one inline-PTX block (d = 128), the
-// descriptor and TMEM address increments computed inside it.  Used by the
-// known-bound instantiation, where it measured faster (1475 -> 1519 TFLOP/s
-// causal B8 H32 N8192); the other instantiations keep one MMA per statement,
-// which measured faster for them.
-__device__ __forceinline__ void mma_ss_x8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
-  asm volatile(
-      "{\n .reg .pred p0, p1;\n .reg .b64 a1, a2, a3, a4, a5, a6, a7, b1, b2, b3, b4, b5, b6, b7;\n"
-      " setp.ne.b32 p0, %3, %3;\n setp.eq.b32 p1, %3, %3;\n"
-      " add.s64 a1, %1, 2;\n add.s64 a2, %1, 4;\n add.s64 a3, %1, 6;\n add.s64 a4, %1, 1024;\n"
-      " add.s64 a5, %1, 1026;\n add.s64 a6, %1, 1028;\n add.s64 a7, %1, 1030;\n"
-      " add.s64 b1, %2, 2;\n add.s64 b2, %2, 4;\n add.s64 b3, %2, 6;\n add.s64 b4, %2, 1024;\n"
-      " add.s64 b5, %2, 1026;\n add.s64 b6, %2, 1028;\n add.s64 b7, %2, 1030;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, p1;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, p1;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, p1;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], a4, b4, %3, p1;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], a5, b5, %3, p1;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], a6, b6, %3, p1;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], a7, b7, %3, p1;\n}\n" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc)
-      : "memory");
+// One lane of a converged warp (the lowest active one) gets true.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n"
+               : "=r"(pred));
+  return pred != 0;
 }
-__device__ __forceinline__ void mma_ts_x8(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
-                                          uint32_t acc0) {
-  asm volatile(
-      "{\n .reg .pred p0, p1;\n .reg .b32 t1, t2, t3, t4, t5, t6, t7;\n"
-      " .reg .b64 b1, b2, b3, b4, b5, b6, b7;\n"
-      " setp.ne.b32 p0, %4, 0;\n setp.eq.b32 p1, %3, %3;\n"
-      " add.s32 t1, %1, 8;\n add.s32 t2, %1, 16;\n add.s32 t3, %1, 24;\n add.s32 t4, %1, 32;\n"
-      " add.s32 t5, %1, 40;\n add.s32 t6, %1, 48;\n add.s32 t7, %1, 56;\n"
-      " add.s64 b1, %2, 128;\n add.s64 b2, %2, 256;\n add.s64 b3, %2, 384;\n add.s64 b4, %2, 512;\n"
-      " add.s64 b5, %2, 640;\n add.s64 b6, %2, 768;\n add.s64 b7, %2, 896;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [t1], b1, %3, p1;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [t2], b2, %3, p1;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [t3], b3, %3, p1;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [t4], b4, %3, p1;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [t5], b5, %3, p1;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [t6], b6, %3, p1;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [t7], b7, %3, p1;\n}\n" ::"r"(d),
-      "r"(a), "l"(b), "r"(idesc), "r"(acc0)
-      : "memory");
-}
-
 
 // Bring a 3-D tile into L2 ahead of its load (no completion to wait for).
 __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1, int c2) {
@@ -396,23 +361,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (q_fill >= 0)
           for (int t = 0; t < 2; ++t) wait_drain(bar(Q_FULL + t), q_fill, 200000000ull);
       }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
+      // The whole warp runs this loop (so its descriptor arithmetic stays
+      // warp-uniform); one elected lane issues each MMA and commit.
       uint32_t slot = 0, ph = 0, qf_ph = 0;
       uint32_t pf_ph[2] = {0, 0}, oe_ph[2] = {0, 0};
       int done = 0;
       bool ok = true;
       const uint64_t dK = sdesc_sw128(0, 16, 1024);     // K-major template (address added)
       const uint64_t dV = sdesc_sw128(0, 16384, 1024);  // MN-major template
+      auto commit = [&](uint32_t b) {
+        if (elect_one()) mma_commit(b);
+        __syncwarp();
+      };
       while (ok) {
-        if (!(ok = wait_one(bar(ITEM_FULL + iq_slot), iq_ph, kSite | 10))) break;
+        if (!(ok = wait_all(bar(ITEM_FULL + iq_slot), iq_ph, kSite | 10))) break;
         const int item = item_q[iq_slot];
-        mbar_arrive(bar(ITEM_EMPTY + iq_slot));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(ITEM_EMPTY + iq_slot));
         iq_advance();
         if (item < 0) break;
         const Item it = item_info(p, item);
         if (it.n_kv == 0) continue;
-        for (int t = 0; t < 2 && ok; ++t) ok = wait_one(bar(Q_FULL + t), qf_ph, kSite | 3);
+        for (int t = 0; t < 2 && ok; ++t) ok = wait_all(bar(Q_FULL + t), qf_ph, kSite | 3);
         if (!ok) break;
         qf_ph ^= 1;
         tc_fence_after();
@@ -421,22 +393,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // O~_t += P_t V_{j-1} once the softmax of tile t has stored P_t
         auto issue_pv = [&](int t) -> bool {
           const uint64_t vdesc = dV + (v_buf >> 4);
-          if (!wait_one(bar(P_FULL + t), pf_ph[t], kSite | 5)) return false;
+          if (!wait_all(bar(P_FULL + t), pf_ph[t], kSite | 5)) return false;
           if (first_pv[t] && done > 0) {
-            if (!wait_one(bar(O_EMPTY + t), oe_ph[t], kSite | 6)) return false;
+            if (!wait_all(bar(O_EMPTY + t), oe_ph[t], kSite | 6)) return false;
             oe_ph[t] ^= 1;
           }
           tc_fence_after();
-          if constexpr (kBounded && D == 128) {
-            mma_ts_x8(tbase + kTmemO + t * 128, tbase + kTmemS + t * 128, vdesc,
-                      idesc_bf16_f32(128, D, true), first_pv[t] ? 0u : 1u);
-          } else {
 #pragma unroll
-            for (int kk = 0; kk < kKeys / 16; ++kk) {  // 16 keys = 8 TMEM columns of P, 2 KB of V
+          for (int kk = 0; kk < kKeys / 16; ++kk) {  // 16 keys = 8 TMEM columns of P, 2 KB of V
+            if (elect_one())
               mma_ts(tbase + kTmemO + t * 128, tbase + kTmemS + t * 128 + kk * 8,
                      vdesc + ((kk * 2048) >> 4), idesc_bf16_f32(128, D, true),
                      (!first_pv[t] || kk > 0) ? 1u : 0u);
-            }
+            __syncwarp();
           }
           pf_ph[t] ^= 1;
           first_pv[t] = false;
@@ -444,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         for (int j = 0; ok && j < it.n_kv; ++j) {
           const uint32_t ps = slot;  // pair j: K_j and (j > 0) V_{j-1}
-          if (!(ok = wait_one(bar(KV_FULL + ps), ph, kSite | 4))) break;
+          if (!(ok = wait_all(bar(KV_FULL + ps), ph, kSite | 4))) break;
           if (++slot == kPairs) { slot = 0; ph ^= 1; }
           tc_fence_after();
           const uint64_t kdesc = dK + ((sKV + (2 * ps) * kTileBytes) >> 4);
@@ -452,39 +421,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int t = 0; t < 2 && ok; ++t) {
             if (j > 0 && !(ok = issue_pv(t))) break;
             const uint64_t qdesc = dK + ((sQ + t * kTileBytes) >> 4);
-            if constexpr (kBounded && D == 128) {
-              mma_ss_x8(tbase + kTmemS + t * 128, qdesc, kdesc, kIdescS);
-            } else {
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {  // 16 columns of d = 32 B of a row
-                const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+            for (int kk = 0; kk < D / 16; ++kk) {  // 16 columns of d = 32 B of a row
+              const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+              if (elect_one())
                 mma_ss(tbase + kTmemS + t * 128, qdesc + off, kdesc + off, kIdescS,
                        kk > 0 ? 1u : 0u);
-              }
+              __syncwarp();
             }
-            mma_commit(bar(S_FULL + t));
+            commit(bar(S_FULL + t));
           }
           if (!ok) break;
-          mma_commit(bar(KV_EMPTY + ps));  // pair j read: S(j) and P V_{j-1} issued
-          if (j == it.n_kv - 1) mma_commit(bar(Q_EMPTY));
+          commit(bar(KV_EMPTY + ps));  // pair j read: S(j) and P V_{j-1} issued
+          if (j == it.n_kv - 1) commit(bar(Q_EMPTY));
         }
         if (!ok) break;
         const uint32_t ps = slot;  // the item's last pair: V_{n-1}
-        if (!(ok = wait_one(bar(KV_FULL + ps), ph, kSite | 4))) break;
+        if (!(ok = wait_all(bar(KV_FULL + ps), ph, kSite | 4))) break;
         if (++slot == kPairs) { slot = 0; ph ^= 1; }
         tc_fence_after();
         v_buf = sKV + (2 * ps + 1) * kTileBytes;
         for (int t = 0; t < 2 && ok; ++t) {
           if (!(ok = issue_pv(t))) break;
-          mma_commit(bar(O_FULL + t));
+          commit(bar(O_FULL + t));
         }
         if (!ok) break;
-        mma_commit(bar(KV_EMPTY + ps));
+        commit(bar(KV_EMPTY + ps));
         ++done;
       }
       if (!ok) {  // wait for every MMA already issued before TMEM is released
-        mma_commit(bar(DRAIN));
-        wait_drain(bar(DRAIN), 0, 200000000ull);
+        commit(bar(DRAIN));
+        if (lane == 0) wait_drain(bar(DRAIN), 0, 200000000ull);
+        __syncwarp();
       }
     }
   } else {
@@ -588,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // pass over kNch chunks of kCw columns (S read from TMEM), each chunk
         // two-phase: all scale/subtracts, then kCw independent exp2, then the
         // sums and bf16 packs -- so the MUFU latency is covered
-        constexpr int kCw = ((D == 64 && !kNorm) || kBounded) ? 64 : 32;
+        constexpr int kCw = kNorm ? 32 : 64;
         constexpr int kNch = kKeys / kCw;
         float la[4] = {0.f, 0.f, 0.f, 0.f};
         // a chunk whose sum passes thr moves the reference (see below)
