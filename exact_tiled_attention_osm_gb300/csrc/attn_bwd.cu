@@ -297,28 +297,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (fill_mask >> s & 1u) wait_drain(bar(RING_FULL + s), fill_ph >> s & 1u, 200000000ull);
       wait_drain(bar(RES_FULL), 0, 200000000ull);
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
+    // The whole warp runs this loop (its descriptor arithmetic stays
+    // warp-uniform); one elected lane issues each MMA and commit.
+    auto wait_w = [&](uint32_t bb, uint32_t parity, unsigned site) -> bool {
+      return __all_sync(0xffffffffu, wait_one(bb, parity, site));
+    };
+    auto commit = [&](uint32_t bb) {
+      if (elect_one()) mma_commit(bb);
+      __syncwarp();
+    };
     // S is double-buffered (TMEM columns 0 and 384): order per key tile j is
     // S_{j+1} | dQ += dS_j K_j (after dS_j) | dP_{j+1}, so S_{j+1} runs while
     // the element-wise warps work on tile j.  Every product that overwrites a
     // TMEM region is issued after the product that reads it.
     const uint64_t dKm = sdesc_sw128(0, 16, 1024);      // K-major template
     const uint64_t dMN = sdesc_sw128(0, 16384, 1024);   // MN-major template
-    bool ok = wait_one(bar(RES_FULL), 0, kSiteQ | 2);
+    bool ok = wait_w(bar(RES_FULL), 0, kSiteQ | 2);
     uint32_t kslot = 0, kph = 0, vph = 0, df_ph = 0;
     if (ok) {
       tc_fence_after();
       const uint64_t qdesc = dKm + (sQ >> 4), dodesc = dKm + (sDO >> 4);
       auto next_k = [&](uint32_t& s_out) -> bool {  // K slots in fill order
         s_out = kslot;
-        const bool r = wait_one(bar(RING_FULL + kslot), kph, kSiteQ | 4);
+        const bool r = wait_w(bar(RING_FULL + kslot), kph, kSiteQ | 4);
         if (++kslot == kKSlots) { kslot = 0; kph ^= 1; }
         return r;
       };
       auto next_v = [&](uint32_t& s_out) -> bool {
         s_out = kVSlot;
-        const bool r = wait_one(bar(RING_FULL + kVSlot), vph, kSiteQ | 4);
+        const bool r = wait_w(bar(RING_FULL + kVSlot), vph, kSiteQ | 4);
         vph ^= 1;
         return r;
       };
@@ -329,9 +338,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-          mma_ss(tsb, qdesc + off, kdesc + off, kIdescKK, kk > 0 ? 1u : 0u);
+          if (elect_one()) mma_ss(tsb, qdesc + off, kdesc + off, kIdescKK, kk > 0 ? 1u : 0u);
+          __syncwarp();
         }
-        mma_commit(bar((jj & 1) ? S_FULL1 : S_FULL));
+        commit(bar((jj & 1) ? S_FULL1 : S_FULL));
       };
       auto issue_dp = [&](uint32_t vs) {  // dP = dO V_j^T; V_j is used by dP_j only
         tc_fence_after();
@@ -339,10 +349,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-          mma_ss(tbase + kTmemDP, dodesc + off, vdesc + off, kIdescKK, kk > 0 ? 1u : 0u);
+          if (elect_one()) mma_ss(tbase + kTmemDP, dodesc + off, vdesc + off, kIdescKK, kk > 0 ? 1u : 0u);
+          __syncwarp();
         }
-        mma_commit(bar(DP_FULL));
-        mma_commit(bar(RING_EMPTY + vs));
+        commit(bar(DP_FULL));
+        commit(bar(RING_EMPTY + vs));
       };
       uint32_t ks = 0, vs = 0;
       if ((ok = next_k(ks))) issue_s(ks, 0);
@@ -355,27 +366,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_s(kn, j + 1);
         }
         // dQ += dS_j K_j once the element-wise warps have written dS_j
-        if (!(ok = wait_one(bar(DS_FULL), df_ph, kSiteQ | 3))) break;
+        if (!(ok = wait_w(bar(DS_FULL), df_ph, kSiteQ | 3))) break;
         df_ph ^= 1;
         tc_fence_after();
         const uint64_t kdesc = dMN + ((sRing + ks * kTileBytes) >> 4);
         const uint32_t tsb = tbase + ((j & 1) ? kTmemAcc1 : kTmemS);
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tbase + kTmemAcc0, tsb + tmem_half_col(kk), kdesc + ((kk * 2048) >> 4), idesc_bf16_f32(128, D, true),
-                 (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(RING_EMPTY + ks));  // K_j is free after this product
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          if (elect_one())
+            mma_ts(tbase + kTmemAcc0, tsb + tmem_half_col(kk), kdesc + ((kk * 2048) >> 4),
+                   idesc_bf16_f32(128, D, true), (j > 0 || kk > 0) ? 1u : 0u);
+          __syncwarp();
+        }
+        commit(bar(RING_EMPTY + ks));  // K_j is free after this product
         if (more) {
           if (!(ok = next_v(vs))) break;
           issue_dp(vs);
         }
         ks = kn;
       }
-      if (ok) mma_commit(bar(O_FULL));
+      if (ok) commit(bar(O_FULL));
     }
     if (!ok) {  // wait for every MMA already issued before TMEM is released
-      mma_commit(bar(DRAIN));
-      wait_drain(bar(DRAIN), 0, 200000000ull);
+      commit(bar(DRAIN));
+      if (lane == 0) wait_drain(bar(DRAIN), 0, 200000000ull);
+      __syncwarp();
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------- P and dS
@@ -563,15 +578,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (fill_mask >> s & 1u) wait_drain(bar(RING_FULL + s), fill_ph >> s & 1u, 200000000ull);
       wait_drain(bar(RES_FULL), 0, 200000000ull);
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
+    // The whole warp runs this loop (its descriptor arithmetic stays
+    // warp-uniform); one elected lane issues each MMA and commit.
+    auto wait_w = [&](uint32_t bb, uint32_t parity, unsigned site) -> bool {
+      return __all_sync(0xffffffffu, wait_one(bb, parity, site));
+    };
+    auto commit = [&](uint32_t bb) {
+      if (elect_one()) mma_commit(bb);
+      __syncwarp();
+    };
     // Order per query tile i: S_i, dP_i | dV_i (after P_i) | S_{i+1} | dK_i
     // (after dS_i) | dP_{i+1}.  Each element-wise phase overlaps two products,
     // and every product that overwrites a TMEM region is issued after the
     // product that reads it (the tensor pipe runs them in issue order).
     const uint64_t dKm = sdesc_sw128(0, 16, 1024);
     const uint64_t dMN = sdesc_sw128(0, 16384, 1024);
-    bool ok = wait_one(bar(RES_FULL), 0, kSiteK | 2);
+    bool ok = wait_w(bar(RES_FULL), 0, kSiteK | 2);
     uint32_t slot = 0, ph = 0, pf_ph = 0, df_ph = 0;
     if (ok) {
       tc_fence_after();
@@ -579,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // pair p holds Q_i in slot 2p and dO_i in slot 2p + 1
       auto next_pair = [&](uint32_t& p_out) -> bool {
         p_out = slot;
-        const bool r = wait_one(bar(RING_FULL + slot), ph, kSiteK | 4);
+        const bool r = wait_w(bar(RING_FULL + slot), ph, kSiteK | 4);
         if (++slot == kPairs) { slot = 0; ph ^= 1; }
         return r;
       };
@@ -589,9 +613,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t o16 = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-          mma_ss(tbase + kTmemS, kdesc + o16, qdesc + o16, kIdescKK, kk > 0 ? 1u : 0u);
+          if (elect_one()) mma_ss(tbase + kTmemS, kdesc + o16, qdesc + o16, kIdescKK, kk > 0 ? 1u : 0u);
+          __syncwarp();
         }
-        mma_commit(bar(S_FULL));
+        commit(bar(S_FULL));
       };
       auto issue_dp = [&](uint32_t ds) {  // dP^T = V dO_i^T
         tc_fence_after();
@@ -599,9 +624,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t o16 = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-          mma_ss(tbase + kTmemDP, vdesc + o16, dodesc + o16, kIdescKK, kk > 0 ? 1u : 0u);
+          if (elect_one()) mma_ss(tbase + kTmemDP, vdesc + o16, dodesc + o16, kIdescKK, kk > 0 ? 1u : 0u);
+          __syncwarp();
         }
-        mma_commit(bar(DP_FULL));
+        commit(bar(DP_FULL));
       };
       uint32_t pc = 0;
       if ((ok = next_pair(pc))) {
@@ -613,36 +639,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t qs = 2 * pc, ds = 2 * pc + 1;
         uint32_t pn = 0;
         // dV += P_i^T dO_i once the element-wise warps have written P_i
-        if (!(ok = wait_one(bar(P_FULL), pf_ph, kSiteK | 3))) break;
+        if (!(ok = wait_w(bar(P_FULL), pf_ph, kSiteK | 3))) break;
         pf_ph ^= 1;
         tc_fence_after();
         const uint64_t dod = dMN + ((sRing + ds * kTileBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tbase + kTmemAcc0, tbase + kTmemS + tmem_half_col(kk), dod + ((kk * 2048) >> 4),
-                 idesc_bf16_f32(128, D, true), (i > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          if (elect_one())
+            mma_ts(tbase + kTmemAcc0, tbase + kTmemS + tmem_half_col(kk), dod + ((kk * 2048) >> 4),
+                   idesc_bf16_f32(128, D, true), (i > 0 || kk > 0) ? 1u : 0u);
+          __syncwarp();
+        }
         if (more) {
           if (!(ok = next_pair(pn))) break;
           issue_s(2 * pn);
         }
         // dK += dS_i^T Q_i once they have written dS_i
-        if (!(ok = wait_one(bar(DS_FULL), df_ph, kSiteK | 7))) break;
+        if (!(ok = wait_w(bar(DS_FULL), df_ph, kSiteK | 7))) break;
         df_ph ^= 1;
         tc_fence_after();
         const uint64_t qd = dMN + ((sRing + qs * kTileBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tbase + kTmemAcc1, tbase + kTmemDP + tmem_half_col(kk), qd + ((kk * 2048) >> 4),
-                 idesc_bf16_f32(128, D, true), (i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(RING_EMPTY + pc));  // Q_i and dO_i are free after dK_i
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          if (elect_one())
+            mma_ts(tbase + kTmemAcc1, tbase + kTmemDP + tmem_half_col(kk), qd + ((kk * 2048) >> 4),
+                   idesc_bf16_f32(128, D, true), (i > 0 || kk > 0) ? 1u : 0u);
+          __syncwarp();
+        }
+        commit(bar(RING_EMPTY + pc));  // Q_i and dO_i are free after dK_i
         if (more) issue_dp(2 * pn + 1);
         pc = pn;
       }
-      if (ok) mma_commit(bar(O_FULL));
+      if (ok) commit(bar(O_FULL));
     }
     if (!ok) {
-      mma_commit(bar(DRAIN));
-      wait_drain(bar(DRAIN), 0, 200000000ull);
+      commit(bar(DRAIN));
+      if (lane == 0) wait_drain(bar(DRAIN), 0, 200000000ull);
+      __syncwarp();
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------- P^T and dS^T

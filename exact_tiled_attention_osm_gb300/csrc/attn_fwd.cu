@@ -123,14 +123,6 @@ constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);  // Q, K both K-ma
 constexpr unsigned kSite = 0x01000000u;
 
 
-// One lane of a converged warp (the lowest active one) gets true.
-__device__ __forceinline__ bool elect_one() {
-  uint32_t pred = 0;
-  asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n"
-               : "=r"(pred));
-  return pred != 0;
-}
-
 // Bring a 3-D tile into L2 ahead of its load (no completion to wait for).
 __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1, int c2) {
   asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
