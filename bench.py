@@ -44,8 +44,11 @@ CSRC = os.path.join(ROOT, "exact_tiled_attention_osm_gb300", "csrc")
 # operation), valid only for the kernel sources it was captured on (sha256 of
 # the listed files, concatenated); None until captured on the current source.
 KERNEL_TRAFFIC = {
-    "attn_fwd_kernel": {"bytes_per_launch": None, "sources": ["attn_fwd.cu", "ptx.cuh"],
-                        "source_sha256": None},
+    # attn_fwd_kernel<false, 128>, causal+padding B8 H32 N8192: read 1,328,141,312
+    # + write 520,573,440
+    "attn_fwd_kernel": {"bytes_per_launch": 1_328_141_312 + 520_573_440,
+                        "sources": ["attn_fwd.cu", "ptx.cuh"],
+                        "source_sha256": "78b3f41cf79707d333308a4645e06da156877ad3f9b5e83a12b2d74304cff8fa"},
     # softmax_rows_cluster<8>, 4096 x 32768: read 536,905,216 + write 483,361,536
     "softmax_rows": {"bytes_per_launch": 536_905_216 + 483_361_536,
                      "sources": ['softmax_rows.cu', 'exp_le0.cuh', 'ptx.cuh'],
