@@ -49,15 +49,15 @@ KERNEL_TRAFFIC = {
     "attn_fwd_kernel": {"bytes_per_launch": 1_328_141_312 + 520_573_440,
                         "sources": ["attn_fwd.cu", "ptx.cuh"],
                         "source_sha256": "78b3f41cf79707d333308a4645e06da156877ad3f9b5e83a12b2d74304cff8fa"},
-    # softmax_rows_cluster<8>, 4096 x 32768: read 536,905,216 + write 483,361,536
-    "softmax_rows": {"bytes_per_launch": 536_905_216 + 483_361_536,
-                     "sources": ['softmax_rows.cu', 'exp_le0.cuh', 'ptx.cuh'],
-                     "source_sha256": "04b2b74e40e3199b82f751e4a512ae8f3a306df9f5f59e3295a67a3b36aeb1e3"},
-    # decode_split_kernel read 17,360,807,936 + write 11,566,848;
-    # merge_kernel read 17,051,648 + write 0
-    "decode_splitkv": {"bytes_per_launch": 17_360_807_936 + 11_566_848 + 17_051_648,
-                       "sources": ['decode.cu', 'ptx.cuh'],
-                       "source_sha256": "2b14b3572fac049d7522e60cafb613da511765ee36992c23d4a268644360114f"},
+    # softmax_rows_cluster<8>, 4096 x 32768: read 536,903,936 + write 481,946,624
+    "softmax_rows": {"bytes_per_launch": 536_903_936 + 481_946_624,
+                     "sources": ["softmax_rows.cu", "exp_le0.cuh", "ptx.cuh"],
+                     "source_sha256": "f26deedb70ff2c33945d2b1187ef07ea2df1b853850ccba0766555ba1420fdc7"},
+    # decode_split_kernel read 17,361,528,832 + write 11,587,072;
+    # merge_kernel read 17,052,416 + write 0
+    "decode_splitkv": {"bytes_per_launch": 17_361_528_832 + 11_587_072 + 17_052_416,
+                       "sources": ["decode.cu", "ptx.cuh"],
+                       "source_sha256": "cd011ed15a5ef9a887da19a75f99e85d474d41deac48210d48db169d591f3bdd"},
 }
 
 

@@ -78,7 +78,7 @@ constexpr int kMaxCluster = 8;
 // One cluster of `nct` CTAs per row; CTA `rank` owns float4 columns
 // [rank*kThreads*V, (rank+1)*kThreads*V) of the row, V per thread.
 template <int V>
-__global__ void __launch_bounds__(kThreads) softmax_rows_cluster(const float* __restrict__ x,
+__global__ void __launch_bounds__(kThreads, 5) softmax_rows_cluster(const float* __restrict__ x,
                                                                   float* __restrict__ y,
                                                                   int cols) {
   __shared__ float2 warp_ml[kWarps];
