@@ -692,19 +692,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 2l, 2l+1 of its half), so only __syncwarp is needed; the next tile's
     // values load while this one runs.
     float* colw = col + (warp - 4) * kColFloats;
+    // The raw lse and D are loaded a tile ahead and converted where they are
+    // staged, so the global loads' latency is never waited on.
     auto col_vals = [&](int i, float (&l2)[2], float (&dd)[2]) {
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int q = (qt_first + i) * kTile + 64 * hh + 2 * lane + u;
-        // stored negated: -lse2 and -D enter packed adds directly
-        if (q < p.Nq) {
-          l2[u] = -p.lse[hrow + q] * kLog2e;
-          if (!(l2[u] < kPosInf)) l2[u] = kNegInf;  // a query with no visible key: P = 0
-          dd[u] = -p.delta[hrow + q];
-        } else {
-          l2[u] = kNegInf;
-          dd[u] = 0.f;
-        }
+        const bool in = q < p.Nq;
+        l2[u] = in ? p.lse[hrow + q] : kNegInf;
+        dd[u] = in ? p.delta[hrow + q] : 0.f;
       }
     };
     float nl2[2], nd[2];
@@ -715,8 +711,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* cl = colw + (i & 1) * kTile;  // [lse2 | D] x 64 columns
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        cl[2 * lane + u] = nl2[u];
-        cl[kTile / 2 + 2 * lane + u] = nd[u];
+        // stored negated: -lse2 and -D enter packed adds directly; a query
+        // with no visible key (lse -inf) gets -lse2 = -inf, so P = 0
+        const float nl = -nl2[u] * kLog2e;
+        cl[2 * lane + u] = nl < kPosInf ? nl : kNegInf;
+        cl[kTile / 2 + 2 * lane + u] = -nd[u];
       }
       __syncwarp();
       if (i + 1 < n_q) col_vals(i + 1, nl2, nd);
