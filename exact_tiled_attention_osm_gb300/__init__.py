@@ -40,7 +40,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libosm.so")
 
 (OSM_OK, OSM_ERR_INVALID_VALUE, OSM_ERR_UNSUPPORTED, OSM_ERR_CUDA, OSM_ERR_TIMEOUT,
- OSM_ERR_CONFLICT) = range(6)
+ OSM_ERR_CONFLICT, OSM_ERR_INDEX) = range(7)
 OSM_F32, OSM_BF16 = 0, 1
 
 # exported names and their C signatures (include/osm.h)
@@ -439,6 +439,6 @@ def device_status(device=None) -> int:
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     with torch.cuda.device(dev):
         st = lib.osm_device_status(torch.cuda.current_stream(dev).cuda_stream, ctypes.byref(w))
-    if st not in (OSM_OK, OSM_ERR_TIMEOUT, OSM_ERR_CONFLICT):
+    if st not in (OSM_OK, OSM_ERR_TIMEOUT, OSM_ERR_CONFLICT, OSM_ERR_INDEX):
         raise OsmError(st, "osm_device_status")
     return int(w.value)

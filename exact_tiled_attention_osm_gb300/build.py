@@ -2,6 +2,9 @@
 
 Each .cu file compiles on its own thread; the objects link into one shared
 library next to this file.  A stamp of the sources and flags skips rebuilds.
+build(checked=True) builds libosm_checked.so instead: the same library
+compiled with OSM_CHECKED, whose kernels check the global indices they
+compute and report one out of range as OSM_ERR_INDEX (for tests).
 """
 from __future__ import annotations
 
@@ -18,6 +21,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libosm.so")
+BUILD_CHECKED = os.path.join(HERE, "_build_checked")
+LIB_CHECKED = os.path.join(HERE, "libosm_checked.so")
 
 SOURCES = ["api.cu", "attn_fwd.cu", "attn_bwd.cu", "softmax_rows.cu", "softmax_topk.cu", "decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -32,31 +37,33 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _stamp() -> str:
+def _stamp(extra=()) -> str:
     h = hashlib.sha256()
     for name in sorted(os.listdir(CSRC)):
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode() + f.read())
     with open(os.path.join(INCLUDE, "osm.h"), "rb") as f:
         h.update(f.read())
-    h.update(" ".join(ARCH + CFLAGS).encode())
+    h.update(" ".join(ARCH + CFLAGS + list(extra)).encode())
     h.update(os.uname().machine.encode())
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    stamp = _stamp()
-    stamp_file = os.path.join(BUILD, "stamp")
-    if not force and os.path.exists(LIB) and os.path.exists(stamp_file):
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    extra = ["-DOSM_CHECKED"] if checked else []
+    build_dir, lib = (BUILD_CHECKED, LIB_CHECKED) if checked else (BUILD, LIB)
+    stamp = _stamp(extra)
+    stamp_file = os.path.join(build_dir, "stamp")
+    if not force and os.path.exists(lib) and os.path.exists(stamp_file):
         with open(stamp_file) as f:
             if f.read() == stamp:
-                return LIB
-    os.makedirs(BUILD, exist_ok=True)
+                return lib
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
-        cmd = [cc, *ARCH, *CFLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
+        cmd = [cc, *ARCH, *CFLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
@@ -66,15 +73,15 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with ThreadPoolExecutor(len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     with open(stamp_file, "w") as f:
         f.write(stamp)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, checked="--checked" in sys.argv))

@@ -21,7 +21,7 @@ inline osm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? OSM_OK : 
 
 extern "C" {
 
-int osm_abi_version(void) { return 102; }
+int osm_abi_version(void) { return 103; }
 
 const char* osm_status_string(osm_status st) {
   switch (st) {
@@ -32,6 +32,8 @@ const char* osm_status_string(osm_status st) {
     case OSM_ERR_TIMEOUT: return "OSM_ERR_TIMEOUT: a bounded device-side wait ran out";
     case OSM_ERR_CONFLICT:
       return "OSM_ERR_CONFLICT: two forward launches in flight shared a work-item counter";
+    case OSM_ERR_INDEX:
+      return "OSM_ERR_INDEX: a checked build found a global index out of range";
   }
   return "unknown osm_status";
 }
@@ -263,8 +265,13 @@ osm_status osm_device_status(osm_stream_t stream, uint32_t* word) {
   e = osm::read_and_clear_bwd_error(&wb);
   if (e != cudaSuccess) return OSM_ERR_CUDA;
   if (*word == 0) *word = wb;
+  uint32_t wd = 0;  // the decode kernels' index-check word (checked builds)
+  e = osm::read_and_clear_decode_check(&wd);
+  if (e != cudaSuccess) return OSM_ERR_CUDA;
+  if (*word == 0) *word = wd;
   if (*word == 0) return OSM_OK;
-  return (*word >> 24) == 0x0Cu ? OSM_ERR_CONFLICT : OSM_ERR_TIMEOUT;
+  const uint32_t top = *word >> 24;
+  return top == 0x0Cu ? OSM_ERR_CONFLICT : (top == 0x0Eu ? OSM_ERR_INDEX : OSM_ERR_TIMEOUT);
 }
 
 }  // extern "C"

@@ -92,6 +92,7 @@ constexpr uint32_t kIdescKK = idesc_bf16_f32(128, 128, false);  // both operands
 
 constexpr unsigned kSiteQ = 0x02000000u;   // error-word sites of the dQ kernel
 constexpr unsigned kSiteK = 0x03000000u;   // ... and of the dK/dV kernel
+constexpr unsigned kChk = 0x0E040000u;     // index checks of an OSM_CHECKED build
 
 struct Params {
   int B, H, Nq, Nk;
@@ -217,7 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (n_kv == 0) {  // no visible key for any row of the tile: dQ = 0
     if (warp >= 4 && warp < 8) {
       const int row = q0 + 32 * (warp - 4) + lane;
-      if (row < p.Nq) zero_row_bf16<D>(p.dq + (static_cast<int64_t>(bh) * p.Nq + row) * D);
+      if (row < p.Nq && checked(bh < p.B * p.H, p.err, kChk | 1))
+        zero_row_bf16<D>(p.dq + (static_cast<int64_t>(bh) * p.Nq + row) * D);
     }
     return;
   }
@@ -463,11 +465,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       tc_fence_after();
       const int row0 = row - lane;  // the warp's first query row
-      store_rows_bf16_staged<D>(
-          tbase + lane_off + kTmemAcc0, p.scale,
-          p.dq + (static_cast<int64_t>(bh) * p.Nq + row0) * D, min(32, p.Nq - row0),
-          hh * (D / 64), (hh + 1) * (D / 64),
-          reinterpret_cast<uint4*>(smem + kSmemStage + (warp - 4) * kStageBytes));
+      // the rows written: [row0, row0 + min(32, Nq - row0)), none when the
+      // warp's rows all lie past Nq
+      if (checked(bh < p.B * p.H && row0 >= 0, p.err, kChk | 2))
+        store_rows_bf16_staged<D>(
+            tbase + lane_off + kTmemAcc0, p.scale,
+            p.dq + (static_cast<int64_t>(bh) * p.Nq + row0) * D, min(32, p.Nq - row0),
+            hh * (D / 64), (hh + 1) * (D / 64),
+            reinterpret_cast<uint4*>(smem + kSmemStage + (warp - 4) * kStageBytes));
     }
   }
   tc_fence_before();
@@ -508,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (n_q == 0) {  // every key of the tile is invisible to every query: dK = dV = 0
     if (warp >= 4 && warp < 8) {
       const int key = k0 + 32 * (warp - 4) + lane;
-      if (key < p.Nk) {
+      if (key < p.Nk && checked(bh < p.B * p.H, p.err, kChk | 3)) {
         const int64_t g = (static_cast<int64_t>(bh) * p.Nk + key) * D;
         zero_row_bf16<D>(p.dk + g);
         zero_row_bf16<D>(p.dv + g);
@@ -800,7 +805,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int key0 = key - lane;  // the warp's first key row
       const int64_t g = (static_cast<int64_t>(bh) * p.Nk + key0) * D;
       uint4* stage = reinterpret_cast<uint4*>(smem + kSmemStage + (warp - 4) * kStageBytes);
-      if (hh == 0)
+      if (!checked(bh < p.B * p.H && key0 >= 0, p.err, kChk | 4)) {  // rows as for dQ
+      } else if (hh == 0)
         store_rows_bf16_staged<D>(tbase + lane_off + kTmemAcc0, 1.f, p.dv + g,
                                   min(32, p.Nk - key0), 0, D / 32, stage);
       else

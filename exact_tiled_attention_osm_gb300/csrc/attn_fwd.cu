@@ -119,8 +119,10 @@ constexpr uint32_t kTmemO = 256;
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);  // Q, K both K-major
 
-// error-word sites (kernel id 1 in the top byte)
+// error-word sites (kernel id 1 in the top byte); index checks of an
+// OSM_CHECKED build use 0x0E01xxxx
 constexpr unsigned kSite = 0x01000000u;
+constexpr unsigned kChk = 0x0E010000u;
 
 
 // Bring a 3-D tile into L2 ahead of its load (no completion to wait for).
@@ -268,6 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int loaded = 0;
       bool ok = true;
       auto publish = [&](int item) -> bool {
+        if (!checked(item >= -1 && item < p.num_items, p.err, kChk | 1)) item = -1;
         if (!wait_one(bar(ITEM_EMPTY + iq_slot), iq_ph ^ 1, kSite | 9)) return false;
         item_q[iq_slot] = item;
         mbar_arrive(bar(ITEM_FULL + iq_slot));
@@ -306,6 +309,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           return publish(item);
         };
         if (it.n_kv > 0) {
+          // the copies' coordinates (out-of-range rows read zeros, so these
+          // only record a fault): the head and the last key tile
+          checked(it.bh < p.B * p.H && (it.n_kv - 1) * kKeys < p.Nk, p.err, kChk | 2);
           if (loaded > 0) {
             if (!(ok = wait_one(bar(Q_EMPTY), qe_ph, kSite | 1))) break;
             qe_ph ^= 1;
@@ -468,8 +474,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = it.q0 + t * kRows + 32 * wq + lane;
       const bool row_ok = row < p.Nq;
       const int64_t orow = static_cast<int64_t>(it.bh) * p.Nq + row;
+      const int64_t n_rows = static_cast<int64_t>(p.B) * p.H * p.Nq;
       if (it.n_kv == 0) {
-        if (row_ok) {
+        if (row_ok && checked(orow < n_rows, p.err, kChk | 3)) {
           uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D);
 #pragma unroll
           for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
@@ -748,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const int r = 8 * g + srow;  // row of the warp this lane stores
-          if (row - lane + r < p.Nq) {
+          if (row - lane + r < p.Nq && checked(orow0 + r < n_rows, p.err, kChk | 4)) {
             uint4* dst = reinterpret_cast<uint4*>(p.o + (orow0 + r) * D + 32 * c);
             dst[lane & 3] = stage[r * 4 + (lane & 3)];
           }
@@ -758,7 +765,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(O_EMPTY + t));
-      if (row_ok) p.lse[orow] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : kNegInf;
+      if (row_ok && checked(orow < n_rows, p.err, kChk | 5))
+        p.lse[orow] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : kNegInf;
     }
   }
 

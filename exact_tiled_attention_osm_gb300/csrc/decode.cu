@@ -78,6 +78,11 @@ struct Workspace {
   float* l;
   float* o;
 };
+
+// Index faults found by an OSM_CHECKED build (0x0E02xxxx); read and cleared
+// by osm_device_status.
+__device__ unsigned int g_chk_word;
+constexpr unsigned kChk = 0x0E020000u;
 // Running summaries extended in place by the append form of the split kernel.
 struct AppendState {
   float* m;               // [rows] natural-log units
@@ -139,7 +144,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const int j = kb + r * KPP + grp;
-      if (j < k_end) {
+      if (j < k_end && ptx::checked(j >= 0 && j < Nk, &g_chk_word, kChk | 1)) {
         ku[r] = __ldcs(kr + static_cast<int64_t>(j) * LPK + sl);
         vu[r] = __ldcs(vr + static_cast<int64_t>(j) * LPK + sl);
       } else {
@@ -210,6 +215,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(
     Lt += sm_l[w] * wgt[w];
   }
   const int64_t p = static_cast<int64_t>(s) * gridDim.y * gridDim.z + row;
+  if (!ptx::checked(p < static_cast<int64_t>(S) * gridDim.y * gridDim.z, &g_chk_word, kChk | 2)) return;
   for (int c = threadIdx.x; c < D; c += kWarps * 32) {
     float o = 0.f;
 #pragma unroll
@@ -290,6 +296,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ mp
   const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
+  if (!ptx::checked(S > 0 && lane * PER + PER <= D, &g_chk_word, kChk | 3)) return;
   float M = kNegInf;
   for (int s = 0; s < S; ++s) M = fmaxf(M, mpart[s * rows + row]);
   float l = 0.f, o[PER];
@@ -452,6 +459,19 @@ cudaError_t launch_decode_splitkv_noalloc(osm_dtype dt, const void* q, const voi
   cudaError_t e = noalloc_scratch_address(&scratch);
   if (e != cudaSuccess) return e;
   return launch_decode_splitkv(dt, q, k, v, o, lse, B, H, Nk, d, scale, key_len, S, scratch, s);
+}
+
+cudaError_t read_and_clear_decode_check(uint32_t* word) {
+  unsigned int w = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&w, g_chk_word, sizeof(w));
+  if (e != cudaSuccess) return e;
+  if (w != 0) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_chk_word, &zero, sizeof(zero));
+    if (e != cudaSuccess) return e;
+  }
+  *word = w;
+  return cudaSuccess;
 }
 
 size_t decode_append_workspace_bytes(int B, int H, int d, int S) {

@@ -24,6 +24,8 @@ cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o
                             const int32_t* key_len, float score_bound, bool normalised,
                             cudaStream_t s, bool* tmap_ok);
 cudaError_t read_and_clear_device_error(cudaStream_t s, uint32_t* word);
+// decode.cu: the index-check word of a build compiled with OSM_CHECKED
+cudaError_t read_and_clear_decode_check(uint32_t* word);
 cudaError_t launch_bounded_wait_selftest(cudaStream_t s);
 
 // attn_bwd.cu

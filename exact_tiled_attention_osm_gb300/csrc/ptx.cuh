@@ -87,6 +87,25 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64
   return true;
 }
 
+// ----------------------------------------------------------------- OSM_CHECKED
+// A build with -DOSM_CHECKED checks the global indices that are not
+// guaranteed by construction alone: a failed check records `site` (top byte
+// 0x0E) in the file's device error word, which osm_device_status reports as
+// OSM_ERR_INDEX, and the caller skips the access.  In the normal build the
+// check is the constant true and compiles away.
+#ifdef OSM_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+__device__ __forceinline__ bool checked(bool in_range, unsigned int* err_word, unsigned int site) {
+  if constexpr (kChecked) {
+    if (!in_range) atomicCAS(err_word, 0u, site);
+    return in_range;
+  }
+  return true;
+}
+
 // One lane of a converged warp (the lowest active one) gets true.
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred = 0;

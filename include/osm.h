@@ -47,8 +47,10 @@ typedef enum {
   OSM_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement (e.g. d) */
   OSM_ERR_CUDA = 3,          /* a CUDA launch or runtime call failed */
   OSM_ERR_TIMEOUT = 4,       /* a bounded device-side wait ran out (osm_device_status) */
-  OSM_ERR_CONFLICT = 5       /* two forward launches in flight shared a work-item
+  OSM_ERR_CONFLICT = 5,      /* two forward launches in flight shared a work-item
                                 counter (osm_device_status; see osm_attn_fwd) */
+  OSM_ERR_INDEX = 6          /* a build with OSM_CHECKED found a global index out of
+                                range and skipped the access (osm_device_status) */
 } osm_status;
 
 typedef enum { OSM_F32 = 0, OSM_BF16 = 1 } osm_dtype;
@@ -382,7 +384,10 @@ const char *osm_status_string(osm_status status);
  * device's error word that bounded waits write.  *word = 0 means no device
  * wait ran out since the last call; otherwise it identifies the site: a
  * word whose top byte is 0x0C is a shared work-item counter (return value
- * OSM_ERR_CONFLICT), any other a bounded wait that ran out (OSM_ERR_TIMEOUT).
+ * OSM_ERR_CONFLICT), 0x0E an index found out of range by a build compiled
+ * with OSM_CHECKED (OSM_ERR_INDEX; such a build checks the global indices
+ * its kernels compute and skips an access that would leave its tensor), any
+ * other a bounded wait that ran out (OSM_ERR_TIMEOUT).
  * Returns OSM_ERR_CUDA if the synchronisation itself fails.  Not a hot-path
  * call.
  */

@@ -47,11 +47,11 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    for st in range(6):
+    for st in range(7):
         s = osm.status_string(st)
         assert s.startswith("OSM_")
     assert "unknown" in osm.status_string(99)
-    assert lib.osm_abi_version() == 102
+    assert lib.osm_abi_version() == 103
 
 
 def test_workspace_bytes_formula(lib):
@@ -242,3 +242,14 @@ def test_binding_refuses_cpu_tensors():
 
 def test_device_status_rejects_null(lib):
     assert lib.osm_device_status(None, None) == osm.OSM_ERR_INVALID_VALUE
+
+
+def test_checked_build_exports_the_same_symbols():
+    """The OSM_CHECKED build compiles (here, without a GPU) and exports every
+    function the header declares."""
+    from exact_tiled_attention_osm_gb300 import build
+    path = build.build(checked=True)
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT (osm_[a-z0-9_]+)\b", out))
+    assert set(declared_functions()) <= exported
