@@ -44,20 +44,20 @@ CSRC = os.path.join(ROOT, "exact_tiled_attention_osm_gb300", "csrc")
 # operation), valid only for the kernel sources it was captured on (sha256 of
 # the listed files, concatenated); None until captured on the current source.
 KERNEL_TRAFFIC = {
-    # attn_fwd_kernel<false, 128>, causal+padding B8 H32 N8192: read 1,328,141,312
-    # + write 520,573,440
-    "attn_fwd_kernel": {"bytes_per_launch": 1_328_141_312 + 520_573_440,
+    # attn_fwd_kernel<false, 128>, causal+padding B8 H32 N8192: read 1,327,613,952
+    # + write 520,226,048
+    "attn_fwd_kernel": {"bytes_per_launch": 1_327_613_952 + 520_226_048,
                         "sources": ["attn_fwd.cu", "ptx.cuh"],
-                        "source_sha256": "78b3f41cf79707d333308a4645e06da156877ad3f9b5e83a12b2d74304cff8fa"},
-    # softmax_rows_cluster<8>, 4096 x 32768: read 536,903,936 + write 481,946,624
-    "softmax_rows": {"bytes_per_launch": 536_903_936 + 481_946_624,
+                        "source_sha256": "33602751bdb14771f17043c119c1d603f657bc91ad6e29f608b979c1017aa4e4"},
+    # softmax_rows_cluster<8>, 4096 x 32768: read 536,902,400 + write 482,214,144
+    "softmax_rows": {"bytes_per_launch": 536_902_400 + 482_214_144,
                      "sources": ["softmax_rows.cu", "exp_le0.cuh", "ptx.cuh"],
-                     "source_sha256": "f26deedb70ff2c33945d2b1187ef07ea2df1b853850ccba0766555ba1420fdc7"},
-    # decode_split_kernel read 17,361,528,832 + write 11,587,072;
-    # merge_kernel read 17,052,416 + write 0
-    "decode_splitkv": {"bytes_per_launch": 17_361_528_832 + 11_587_072 + 17_052_416,
+                     "source_sha256": "0c9eec72170dd51eea0a65ee31f6a71e07ac7b4677f07131bb70e57ee562d491"},
+    # decode_split_kernel read 17,360,707,328 + write 11,661,312;
+    # merge_kernel read 17,050,368 + write 0
+    "decode_splitkv": {"bytes_per_launch": 17_360_707_328 + 11_661_312 + 17_050_368,
                        "sources": ["decode.cu", "ptx.cuh"],
-                       "source_sha256": "cd011ed15a5ef9a887da19a75f99e85d474d41deac48210d48db169d591f3bdd"},
+                       "source_sha256": "2c4a67054d27031ea9697220946b0f37ca58359852568d502f2e77ad0c255509"},
 }
 
 
