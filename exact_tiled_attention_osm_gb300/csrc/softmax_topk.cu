@@ -40,6 +40,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegInf = -__builtin_huge_valf();
+constexpr float kMaxFloat = 3.402823466e38f;
 constexpr int kNoIndex = 0x7fffffff;  // empty list slot: after every real entry
 
 // the total order of (value, index) pairs
@@ -293,16 +294,17 @@ __global__ void __launch_bounds__(kThreads) softmax_topk_kernel(const float* __r
   const float4* x4 = reinterpret_cast<const float4*>(xr);
   const int64_t f0 = c0 / 4, f1 = c1 / 4;
 
-  // ---- pass 1: (m, l) and the thread maximum
-  float m = kNegInf, l = 0.f;
+  // ---- pass 1: (m, l) and the thread maximum.  m starts at the lowest
+  // finite float rather than -inf, so the updates need no branch: a group of
+  // -inf entries adds exp2(-inf) = 0 and rescales by exp2(0) = 1.
+  float m = -kMaxFloat, l = 0.f;
   float bv = kNegInf;  // K == 1: the thread's best entry (elements arrive in column order)
   int bi = kNoIndex;
   auto best = [&](float v, int j) {
     if constexpr (K == 1) {
-      if (v > bv || bi == kNoIndex) {
-        bv = v;
-        bi = j;
-      }
+      const bool t = v > bv || bi == kNoIndex;
+      bv = t ? v : bv;
+      bi = t ? j : bi;
     }
   };
   auto add1 = [&](float v) {
@@ -327,10 +329,19 @@ __global__ void __launch_bounds__(kThreads) softmax_topk_kernel(const float* __r
     for (; f + 3 * kThreads < f1; f += 4 * kThreads) {  // four 16-byte loads in flight
       const float4 a = x4[f], b = x4[f + kThreads];
       const float4 c = x4[f + 2 * kThreads], d = x4[f + 3 * kThreads];
-      add4(a);
-      add4(b);
-      add4(c);
-      add4(d);
+      {  // the 16 entries' maximum, one rescale of l, 16 terms: one basic block
+        const float4 e[4] = {a, b, c, d};
+        float mg = m;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) mg = fmaxf(mg, fmaxf(fmaxf(e[u].x, e[u].y), fmaxf(e[u].z, e[u].w)));
+        float s = l * ptx::ex2((m - mg) * kLog2e);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          s += (ptx::ex2((e[u].x - mg) * kLog2e) + ptx::ex2((e[u].y - mg) * kLog2e)) +
+               (ptx::ex2((e[u].z - mg) * kLog2e) + ptx::ex2((e[u].w - mg) * kLog2e));
+        l = s;
+        m = mg;
+      }
       if constexpr (K == 1) {
         const float4 e[4] = {a, b, c, d};
 #pragma unroll
@@ -359,7 +370,8 @@ __global__ void __launch_bounds__(kThreads) softmax_topk_kernel(const float* __r
       best(a, static_cast<int>(j));
     }
   }
-  const float tmax = m;  // the running max is the thread's maximum
+  // the running max is the thread's maximum (-inf when it saw only -inf)
+  const float tmax = l > 0.f ? m : kNegInf;
 
   // warp (m, l)
 #pragma unroll
