@@ -494,11 +494,19 @@ __global__ void __launch_bounds__(kThreads) softmax_topk_kernel(const float* __r
         uint32_t msk = 0;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          if (f + u * kThreads >= f1) continue;  // past the slice: no entry
-          msk |= (a[u].x >= kv ? 1u : 0u) << (4 * u);
-          msk |= (a[u].y >= kv ? 2u : 0u) << (4 * u);
-          msk |= (a[u].z >= kv ? 4u : 0u) << (4 * u);
-          msk |= (a[u].w >= kv ? 8u : 0u) << (4 * u);
+          // past the slice: no entry.  Selects instead of a branch measured
+          // 2-5 % faster for k <= 16 and 10 % slower at k = 32.
+          if constexpr (K <= 16) {
+            const uint32_t b = (a[u].x >= kv ? 1u : 0u) | (a[u].y >= kv ? 2u : 0u) |
+                               (a[u].z >= kv ? 4u : 0u) | (a[u].w >= kv ? 8u : 0u);
+            msk |= (f + u * kThreads < f1 ? b : 0u) << (4 * u);
+          } else {
+            if (f + u * kThreads >= f1) continue;
+            msk |= (a[u].x >= kv ? 1u : 0u) << (4 * u);
+            msk |= (a[u].y >= kv ? 2u : 0u) << (4 * u);
+            msk |= (a[u].z >= kv ? 4u : 0u) << (4 * u);
+            msk |= (a[u].w >= kv ? 8u : 0u) << (4 * u);
+          }
         }
         while (__any_sync(0xffffffffu, msk != 0)) {
           float cv = kNegInf;
