@@ -222,14 +222,16 @@ cudaError_t launch_softmax_rows(const float* x, float* y, int64_t rows, int64_t 
   const bool aligned = (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
                        (reinterpret_cast<uintptr_t>(y) % 16 == 0) && (cols % 4 == 0);
   if (aligned && cols <= 131072) {
-    // columns per CTA = kThreads * 4 * V; choose V so one cluster covers the row
+    // columns per CTA = kThreads * 4 * V; one CTA per row while 8 float4 per
+    // thread cover it, else clusters of 8-float4 slices (16 past 8 CTAs)
     int V = 16;
-    for (int cand : {2, 4, 8, 16}) {
-      if ((cols + kThreads * 4 * cand - 1) / (kThreads * 4 * cand) <= 4) {
+    for (int cand : {2, 4, 8}) {
+      if (cols <= kThreads * 4 * cand) {
         V = cand;
         break;
       }
     }
+    if (V == 16 && (cols + kThreads * 32 - 1) / (kThreads * 32) <= 8) V = 8;
     const int per = kThreads * 4 * V;
     const int nct = static_cast<int>((cols + per - 1) / per);
     if (rows * nct <= 0x7fffffffLL) {
