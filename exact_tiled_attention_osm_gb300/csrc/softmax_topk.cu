@@ -370,8 +370,9 @@ __global__ void __launch_bounds__(kThreads) softmax_topk_kernel(const float* __r
       best(a, static_cast<int>(j));
     }
   }
-  // the running max is the thread's maximum (-inf when it saw only -inf)
-  const float tmax = l > 0.f ? m : kNegInf;
+  // the running max is the thread's maximum; -inf when it saw only -inf
+  // (m never moved and nothing was summed)
+  const float tmax = (m > -kMaxFloat || l > 0.f) ? m : kNegInf;
 
   // warp (m, l)
 #pragma unroll
