@@ -49,10 +49,10 @@ KERNEL_TRAFFIC = {
     "attn_fwd_kernel": {"bytes_per_launch": 1_327_613_952 + 520_226_048,
                         "sources": ["attn_fwd.cu", "ptx.cuh"],
                         "source_sha256": "33602751bdb14771f17043c119c1d603f657bc91ad6e29f608b979c1017aa4e4"},
-    # softmax_rows_cluster<8>, 4096 x 32768: read 536,970,752 + write 482,339,328
-    "softmax_rows": {"bytes_per_launch": 536_970_752 + 482_339_328,
+    # softmax_rows_cluster<8>, 4096 x 32768: read 536,902,144 + write 482,932,736
+    "softmax_rows": {"bytes_per_launch": 536_902_144 + 482_932_736,
                      "sources": ["softmax_rows.cu", "exp_le0.cuh", "ptx.cuh"],
-                     "source_sha256": "cbde99650114ec5d0cb31abf593cb5bdc957750c1afaf7bf88f471f5f6668dff"},
+                     "source_sha256": "75f64fc7cf44844ecc1954fa06f9f15d46c1e80fc56aa2f001e6655e385b4a6e"},
     # decode_split_kernel read 17,360,707,328 + write 11,661,312;
     # merge_kernel read 17,050,368 + write 0
     "decode_splitkv": {"bytes_per_launch": 17_360_707_328 + 11_661_312 + 17_050_368,

@@ -269,6 +269,10 @@ osm_status osm_device_status(osm_stream_t stream, uint32_t* word) {
   e = osm::read_and_clear_decode_check(&wd);
   if (e != cudaSuccess) return OSM_ERR_CUDA;
   if (*word == 0) *word = wd;
+  uint32_t ws = 0;  // the row-softmax kernels' word
+  e = osm::read_and_clear_softmax_error(&ws);
+  if (e != cudaSuccess) return OSM_ERR_CUDA;
+  if (*word == 0) *word = ws;
   if (*word == 0) return OSM_OK;
   const uint32_t top = *word >> 24;
   return top == 0x0Cu ? OSM_ERR_CONFLICT : (top == 0x0Eu ? OSM_ERR_INDEX : OSM_ERR_TIMEOUT);

