@@ -131,6 +131,12 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n"
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// a cluster barrier when the row spans several CTAs, else the CTA's own
+// (cheaper; nct is the same in every thread)
+__device__ __forceinline__ void row_sync(int nct) {
+  if (nct > 1) cluster_sync_all();
+  else __syncthreads();
+}
 __device__ __forceinline__ uint32_t cluster_addr(const void* local, uint32_t rank) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
@@ -233,7 +239,7 @@ __device__ __forceinline__ void cluster_topk(List<K>& L, float* s_pv, int* s_pi,
     c_v[lane] = av;
     c_i[lane] = ai;
   }
-  cluster_sync_all();  // every CTA's list is visible to CTA 0
+  row_sync(nct);  // every CTA's list is visible to CTA 0
   if (rank == 0 && warp == 0) {
     for (int q = 1; q < nct; ++q)
       warp_merge_pairs(av, ai, ld_cluster_f32(cluster_addr(&c_v[lane], q)),
@@ -256,7 +262,7 @@ __device__ __forceinline__ void cluster_merge_lists(float& av, int& ai, float* s
     c_v[lane] = av;
     c_i[lane] = ai;
   }
-  cluster_sync_all();  // every CTA's list is visible to CTA 0
+  row_sync(nct);  // every CTA's list is visible to CTA 0
   if (rank == 0 && warp == 0) {
     for (int q = 1; q < nct; ++q)
       warp_merge_pairs(av, ai, ld_cluster_f32(cluster_addr(&c_v[lane], q)),
@@ -568,7 +574,7 @@ __global__ void __launch_bounds__(kThreads) softmax_topk_kernel(const float* __r
       prow[lane] = (Ls > 0.f && v0 != kNegInf) ? exp_le0(v0 - M) * inv : 0.f;
     }
   }
-  cluster_sync_all();  // CTA 0 has read every CTA's shared memory
+  row_sync(nct);  // CTA 0 has read every CTA's shared memory
 }
 
 template <int K>
