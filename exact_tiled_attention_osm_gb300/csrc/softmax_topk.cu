@@ -574,7 +574,7 @@ __global__ void __launch_bounds__(kThreads) softmax_topk_kernel(const float* __r
       prow[lane] = (Ls > 0.f && v0 != kNegInf) ? exp_le0(v0 - M) * inv : 0.f;
     }
   }
-  row_sync(nct);  // CTA 0 has read every CTA's shared memory
+  if (nct > 1) cluster_sync_all();  // CTA 0 has read every CTA's shared memory
 }
 
 template <int K>
