@@ -21,6 +21,7 @@ prints the line with the maximum time over ranks.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import math
@@ -107,7 +108,11 @@ def decode_bytes(B, H, d, key_len, elem=2):
 # ----------------------------------------------------------------- clocks
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi readings every 20 ms; stop() keeps the ones taken inside the
+    timed region (wall clock, from the first launch to the final
+    synchronisation), or the nearest one after its start when the region is
+    shorter than a reading."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -119,12 +124,12 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
 
-    def stop(self):
+    def stop(self, t0=None, t1=None):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -133,24 +138,29 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, smax, reasons, power = [], None, set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for line in out.strip().splitlines():
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax = float(parts[2])
-                power.append(float(parts[3]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]), float(parts[4]),
+                             {nm for nm, val in zip(names, parts[6:10]) if val.lower() == "active"}))
             except ValueError:
                 continue
-            for nm, val in zip(names, parts[5:9]):
-                if val.lower() == "active":
-                    reasons.add(nm)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm),
-                "power_w_max": max(power) if power else None}
+        inside = [r for r in rows if t0 is not None and t0 <= r[0] <= t1]
+        if not inside and t0 is not None:
+            after = [r for r in rows if r[0] >= t0]
+            inside = after[:1]
+        use = inside if inside else rows
+        reasons = set().union(*[r[4] for r in use]) if use else set()
+        return {"sm_mhz": statistics.median([r[1] for r in use]) if use else None,
+                "sm_max_mhz": use[-1][2] if use else None,
+                "reasons": sorted(reasons), "samples": len(use),
+                "samples_in_timed_region": len([r for r in rows if t0 is not None and t0 <= r[0] <= t1]),
+                "power_w_max": max(r[3] for r in use) if use else None}
 
 
 # ----------------------------------------------------------------- the GPU arm
@@ -219,14 +229,16 @@ def gpu_arm(args, rank, world, dev):
     time.sleep(0.3)  # let the sampler take its first reading
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
     start.record(stream)
     for i in range(args.steps):
         step(evs[i])
     end.record(stream)
     torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
     if world > 1:
         torch.distributed.barrier()
-    clocks = clk.stop()
+    clocks = clk.stop(t_wall0, t_wall1)
     total_ms = start.elapsed_time(end)
     t_attn = [e[0].elapsed_time(e[1]) for e in evs]
     t_soft = [e[1].elapsed_time(e[2]) for e in evs]

@@ -63,3 +63,36 @@ def test_reduce_max_two_ranks_gloo():
 
 def test_reduce_max_single_rank_is_identity():
     assert bench.reduce_max({"a": 1.5}, 1, "cpu") == {"a": 1.5}
+
+
+class _FakeProc:
+    def __init__(self, out):
+        self.out = out
+
+    def terminate(self):
+        pass
+
+    def communicate(self, timeout=None):
+        return self.out, ""
+
+
+def test_clock_sampler_keeps_readings_inside_the_timed_region():
+    import datetime
+    base = datetime.datetime(2026, 1, 2, 3, 4, 5)
+    lines = []
+    for i, (mhz, w, pcap) in enumerate([(1500, 150, "Not Active"), (2070, 900, "Not Active"),
+                                        (2070, 1100, "Active"), (1600, 160, "Not Active")]):
+        ts = (base + datetime.timedelta(milliseconds=20 * i)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        lines.append(f"{ts}, 0, {mhz}, 2070, {w}, 0x0, Not Active, Not Active, Not Active, {pcap}")
+    c = bench.ClockSampler(0)
+    c.proc = _FakeProc("\n".join(lines) + "\n")
+    t0 = (base + datetime.timedelta(milliseconds=10)).timestamp()
+    t1 = (base + datetime.timedelta(milliseconds=50)).timestamp()
+    r = c.stop(t0, t1)
+    assert r["samples"] == 2 and r["samples_in_timed_region"] == 2
+    assert r["sm_mhz"] == 2070 and r["power_w_max"] == 1100 and r["reasons"] == ["sw_power_cap"]
+    # a region shorter than the reading interval keeps the first reading after its start
+    c.proc = _FakeProc("\n".join(lines) + "\n")
+    t0 = (base + datetime.timedelta(milliseconds=25)).timestamp()
+    r = c.stop(t0, t0 + 0.001)
+    assert r["samples"] == 1 and r["samples_in_timed_region"] == 0 and r["power_w_max"] == 1100
