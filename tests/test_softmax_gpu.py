@@ -27,7 +27,8 @@ def run(x):
 
 
 @pytest.mark.parametrize("rows,cols", [(1, 1), (3, 4), (5, 7), (2, 1000), (7, 4096), (3, 4100),
-                                       (3, 32768), (2, 65540), (2, 131072), (2, 131076),
+                                       (4, 8192), (3, 8196), (2, 16388), (3, 32768), (2, 65536),
+                                       (2, 65540), (2, 131072), (2, 131076),
                                        (1, 200003), (300, 96), (1, 1 << 22), (70000, 64)])
 def test_shapes(cuda_ok, rows, cols):
     x = W.softmax_logits(seed=rows * 7 + cols, rows=rows, cols=cols)
