@@ -125,6 +125,30 @@ constexpr unsigned kSite = 0x01000000u;
 constexpr unsigned kChk = 0x0E010000u;
 
 
+// Store a 3-D box from shared memory (row-major, no swizzle) to global memory
+// through the tensor map, as one bulk group; rows outside the tensor are not
+// written.  The caller waits (bulk_wait_read) before it rewrites the source.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1,
+                                             int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];\n"
+      "cp.async.bulk.commit_group;" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+// every bulk store this thread issued has read its shared-memory source
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// every bulk store this thread issued has completed
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// generic-proxy writes to shared memory, visible to a bulk copy issued next
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Bring a 3-D tile into L2 ahead of its load (no completion to wait for).
 __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1, int c2) {
   asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
@@ -199,7 +223,8 @@ constexpr unsigned kConflictSite = 0x0C000001u;
 template <bool kBounded, int D, bool kNorm = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const Params p) {
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -732,11 +757,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv = kNorm ? (l > 0.f ? 1.f : 0.f) : (l + corr > 0.f ? 1.f / (l + corr) : 0.f);
       // O = O~ / l in bf16, a 32-column chunk at a time: each thread puts its
-      // row's 64 bytes into the warp's staging area, then the warp stores 8
-      // rows x 64 contiguous bytes per instruction (4 lanes per row segment)
+      // row's 64 bytes into the warp's staging area (32 rows x 64 bytes,
+      // row-major), and one lane hands the 32 x 32 box to the tensor-memory
+      // engine as a bulk store (rows past Nq are not written), so the warp
+      // does not wait for its global stores
       uint4* stage = reinterpret_cast<uint4*>(smem + kSmemStage + (warp - 4) * kStageBytes);
-      const int srow = (lane >> 2);  // this lane's row within each group of 8
-      const int64_t orow0 = static_cast<int64_t>(it.bh) * p.Nq + (row - lane);
+      const uint32_t stage_s = smem_u32(stage);
+      const int row0 = row - lane;  // the warp's first row in its head
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t orr[32];
@@ -748,19 +775,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                     __uint_as_float(orr[2 * e + 1]) * inv);
           pk2[e] = *reinterpret_cast<uint32_t*>(&h2);
         }
+        if (lane == 0) bulk_wait_read();  // the previous box has left the stage
+        __syncwarp();
 #pragma unroll
         for (int e = 0; e < 4; ++e)
           stage[lane * 4 + e] = make_uint4(pk2[4 * e], pk2[4 * e + 1], pk2[4 * e + 2], pk2[4 * e + 3]);
+        fence_proxy_async_smem();
         __syncwarp();
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const int r = 8 * g + srow;  // row of the warp this lane stores
-          if (row - lane + r < p.Nq && checked(orow0 + r < n_rows, p.err, kChk | 4)) {
-            uint4* dst = reinterpret_cast<uint4*>(p.o + (orow0 + r) * D + 32 * c);
-            dst[lane & 3] = stage[r * 4 + (lane & 3)];
-          }
-        }
-        __syncwarp();
+        // (a warp whose rows all lie past Nq stores nothing)
+        if (lane == 0 && row0 < p.Nq && checked(it.bh < p.B * p.H && row0 >= 0, p.err, kChk | 4))
+          tma_store_3d(&tm_o, stage_s, 32 * c, row0, it.bh);
       }
       tc_fence_before();
       __syncwarp();
@@ -770,6 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  if (warp >= 4 && lane == 0) bulk_wait_all();  // the epilogue's bulk stores have completed
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -819,11 +844,12 @@ cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o
         static_cast<__nv_bfloat16*>(o), lse, rows, d);
     return cudaGetLastError();
   }
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   const uint64_t BH = static_cast<uint64_t>(B) * H;
   if (!make_tmap_bf16_3d(&tq, q, d, Nq, BH, 64, kRows) ||
       !make_tmap_bf16_3d(&tk, k, d, Nk, BH, 64, kKeys) ||
-      !make_tmap_bf16_3d(&tv, v, d, Nk, BH, 64, kKeys)) {
+      !make_tmap_bf16_3d(&tv, v, d, Nk, BH, 64, kKeys) ||
+      !make_tmap_bf16_3d(&to, o, d, Nq, BH, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE)) {
     *tmap_ok = false;
     return cudaSuccess;
   }
@@ -892,19 +918,19 @@ cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o
   const bool bounded = std::isfinite(score_bound);
   if (normalised) {
     if (d == 128)
-      attn_fwd_kernel<false, 128, true><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+      attn_fwd_kernel<false, 128, true><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, to, p);
     else
-      attn_fwd_kernel<false, 64, true><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+      attn_fwd_kernel<false, 64, true><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, to, p);
   } else if (d == 128) {
     if (bounded)
-      attn_fwd_kernel<true, 128><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+      attn_fwd_kernel<true, 128><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, to, p);
     else
-      attn_fwd_kernel<false, 128><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+      attn_fwd_kernel<false, 128><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, to, p);
   } else {
     if (bounded)
-      attn_fwd_kernel<true, 64><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+      attn_fwd_kernel<true, 64><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, to, p);
     else
-      attn_fwd_kernel<false, 64><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+      attn_fwd_kernel<false, 64><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, to, p);
   }
   return cudaGetLastError();
 }

@@ -35,9 +35,12 @@ inline MemsetD32Fn memset_d32_fn() {
 }
 
 // A [outer, rows, inner] bf16 tensor (inner contiguous) read in boxes of
-// box_inner x box_rows x 1 with 128-byte swizzle; out-of-range rows read 0.
+// box_inner x box_rows x 1 with 128-byte swizzle (or none, for boxes stored
+// from a plain row-major stage); out-of-range rows read 0 (and are not written
+// by a store).
 inline bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
-                              uint64_t outer, uint32_t box_inner, uint32_t box_rows) {
+                              uint64_t outer, uint32_t box_inner, uint32_t box_rows,
+                              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = tmap_encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {inner, rows, outer};
@@ -45,7 +48,7 @@ inline bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner
   cuuint32_t box[3] = {box_inner, box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
