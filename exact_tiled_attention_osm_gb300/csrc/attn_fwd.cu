@@ -109,7 +109,10 @@ constexpr uint32_t kSmemItems = kSmemAbort + 4;  // int[kItemSlots]: the CTA's i
 // so that the warp's global stores cover whole 64-byte row segments
 constexpr uint32_t kStageBytes = 32 * 64;
 constexpr uint32_t kSmemStage = (kSmemItems + 4 * kItemSlots + 127) / 128 * 128;
-constexpr uint32_t kSmemBytes = kSmemStage + 8 * kStageBytes + 1024;  // + alignment slack
+// two stages per softmax warp, in turn, so a chunk's box need not have left
+// the stage before the next chunk is written
+constexpr uint32_t kSmemBytes = kSmemStage + 2 * 8 * kStageBytes + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 // readers of the item queue: the MMA thread and the eight softmax warps
 constexpr uint32_t kItemReaders = 1 + 8;
 
@@ -136,9 +139,10 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
       "r"(src), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
-// every bulk store this thread issued has read its shared-memory source
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+// every bulk store this thread issued, except the most recent one, has read
+// its shared-memory source
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 // every bulk store this thread issued has completed
 __device__ __forceinline__ void bulk_wait_all() {
@@ -761,11 +765,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // row-major), and one lane hands the 32 x 32 box to the tensor-memory
       // engine as a bulk store (rows past Nq are not written), so the warp
       // does not wait for its global stores
-      uint4* stage = reinterpret_cast<uint4*>(smem + kSmemStage + (warp - 4) * kStageBytes);
-      const uint32_t stage_s = smem_u32(stage);
+      // (formed from the shared array itself, so the stage writes are
+      // shared-memory stores)
+      uint8_t* stage_base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u) +
+                            kSmemStage + (warp - 4) * 2 * kStageBytes;
       const int row0 = row - lane;  // the warp's first row in its head
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
+        uint4* stage = reinterpret_cast<uint4*>(stage_base + (c & 1) * kStageBytes);
+        const uint32_t stage_s = smem_u32(stage);
         uint32_t orr[32];
         tmem_ld_x32(tO + 32 * c, orr);
         uint32_t pk2[16];
@@ -775,7 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                     __uint_as_float(orr[2 * e + 1]) * inv);
           pk2[e] = *reinterpret_cast<uint32_t*>(&h2);
         }
-        if (lane == 0) bulk_wait_read();  // the previous box has left the stage
+        if (lane == 0) bulk_wait_read_1();  // the box written two chunks ago has left this stage
         __syncwarp();
 #pragma unroll
         for (int e = 0; e < 4; ++e)
