@@ -30,6 +30,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -884,12 +885,13 @@ cudaError_t launch_attn_bwd(const void* q, const void* k, const void* v, const v
   cudaError_t e = cudaGetSymbolAddress(&errp, g_bwd_err);
   if (e != cudaSuccess) return e;
   p.err = static_cast<unsigned int*>(errp);
-  static unsigned long long attr_done = 0;
+  // the shared-memory opt-in is per function and per device
+  static std::atomic<unsigned long long> attr_done{0};
   int dev = 0;
   e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
-  if (!(attr_done & bit)) {
+  if (!(attr_done.load() & bit)) {
     for (const void* fn : {reinterpret_cast<const void*>(bwd_dq_kernel<128>),
                            reinterpret_cast<const void*>(bwd_dkdv_kernel<128>),
                            reinterpret_cast<const void*>(bwd_dq_kernel<64>),
@@ -898,7 +900,7 @@ cudaError_t launch_attn_bwd(const void* q, const void* k, const void* v, const v
                                static_cast<int>(kSmemBytes));
       if (e != cudaSuccess) return e;
     }
-    attr_done |= bit;
+    attr_done.fetch_or(bit);
   }
   if (Nk > 0 && Nq > 0) {
     const unsigned g = static_cast<unsigned>(BH * p.n_kt);

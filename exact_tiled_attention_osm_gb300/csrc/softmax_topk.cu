@@ -15,16 +15,19 @@
 //
 // GB300 mapping: one cluster of nct CTAs (256 threads each) per row; CTA r of
 // the cluster streams a contiguous slice of the row with 16-byte loads, four
-// in flight per thread, twice: the first pass forms (m, l) and each thread's
-// maximum, whose k-th largest within the warp (within the CTA for k > 16) is
-// a threshold every top-k entry reaches; the second pass (served mostly from
-// L2, the slice was just read) inserts only entries that beat the warp's
-// filter into the warp's running list of 32 pairs, one per lane, and tightens
-// the filter to the list's k-th entry.  The CTA's lists meet pairwise
-// through shared memory (three rounds for eight warps) and the cluster's in
-// CTA 0 through distributed shared memory, by bitonic merges.  K = 1 needs one pass
-// (each thread's arg-max).  HBM-bound: 4 bytes read per element once from
-// HBM, 8 bytes written per output entry.
+// in flight per thread.  That pass forms (m, l), each thread's maximum and
+// the maximum of each of its groups of 16 entries (kept in shared memory);
+// the k-th largest thread maximum within the warp (within the CTA for
+// k > 16) is a threshold every top-k entry reaches.  Only the groups whose
+// maximum reaches it are read again (from L2, mostly): the warp shares them
+// out one per lane, and the entries that beat the warp's filter enter the
+// warp's running list of 32 pairs, one per lane, by insertion when a round
+// offers few and by a sort and merge when it offers many; the filter tightens
+// to the list's k-th entry.  The CTA's lists meet pairwise through shared
+// memory (three rounds for eight warps) and the cluster's in CTA 0 through
+// distributed shared memory, by bitonic merges.  K = 1 needs one pass (each
+// thread's arg-max).  HBM-bound: 4 bytes read per element once from HBM (plus
+// the few groups read again), 8 bytes written per output entry.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -42,10 +45,29 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kMaxFloat = 3.402823466e38f;
 constexpr int kNoIndex = 0x7fffffff;  // empty list slot: after every real entry
+// K > 1: the maxima of a thread's groups of 16 entries (the four 16-byte
+// loads of one step of the first pass) kept for the second pass; groups past
+// kGroupSlots share slot g mod kGroupSlots (kept as the maximum over them)
+constexpr int kGroupSlots = 16;
 
 // the total order of (value, index) pairs
 __device__ __forceinline__ bool before(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
+}
+
+// position of the n-th (0-based) set bit of m; n < popc(m)
+__device__ __forceinline__ int nth_set_bit(unsigned m, int n) {
+  int pos = 0;
+#pragma unroll
+  for (int w = 16; w > 0; w >>= 1) {
+    const int c = __popc(m & ((1u << w) - 1u));
+    if (n >= c) {
+      n -= c;
+      m >>= w;
+      pos += w;
+    }
+  }
+  return pos;
 }
 
 // K best (value, index) pairs seen so far, sorted by the order above
@@ -249,13 +271,25 @@ __device__ __forceinline__ void cluster_topk(List<K>& L, float* s_pv, int* s_pi,
 
 // The 32 best entries of the cluster from each warp's lane-sorted list (av, ai),
 // lane-sorted in warp 0 of CTA 0; as the tail of cluster_topk.
+// Also merges the warps' (m, l) (s_m, s_l) into the CTA's (c_ml).
 __device__ __forceinline__ void cluster_merge_lists(float& av, int& ai, float* s_pv, int* s_pi,
-                                                    float* c_v, int* c_i, int nct,
+                                                    const float* s_m, const float* s_l,
+                                                    float* c_ml, float* c_v, int* c_i, int nct,
                                                     uint32_t rank) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   s_pv[warp * 32 + lane] = av;
   s_pi[warp * 32 + lane] = ai;
   cta_tree_merge_pairs(s_pv, s_pi);
+  if (threadIdx.x == 32) {  // the CTA's (m, l), read by CTA 0 at the end
+    float M = s_m[0], Ls = s_l[0];
+    for (int w = 1; w < kWarps; ++w) {
+      const float mn = fmaxf(M, s_m[w]);
+      Ls = Ls * rebase(M, mn) + s_l[w] * rebase(s_m[w], mn);
+      M = mn;
+    }
+    c_ml[0] = M;
+    c_ml[1] = Ls;
+  }
   if (warp == 0) {
     av = s_pv[lane];
     ai = s_pi[lane];
@@ -270,24 +304,27 @@ __device__ __forceinline__ void cluster_merge_lists(float& av, int& ai, float* s
   }
 }
 
-// Two passes over the CTA's slice of the row (the second mostly from L2):
-//  1. the online (m, l) and each thread's maximum; the K-th largest thread
-//     maximum of a warp is a threshold T with at least K entries of the warp
-//     >= T, so every entry of the row's top K is >= its warp's T;
-//  2. only entries that beat the warp's filter (T, then the K-th entry of the
-//     warp's running list) enter that list; the warps' lists merge into the
-//     row's top K.  K = 1 needs one pass: each thread's argmax.
+// Two passes over the CTA's slice of the row (the second over a few groups):
+//  1. the online (m, l), each thread's maximum and its groups' maxima; the
+//     K-th largest thread maximum of a warp is a threshold T with at least K
+//     entries of the warp >= T, so every entry of the row's top K is >= its
+//     warp's T, and lies in a group whose maximum is >= T;
+//  2. only entries of those groups that beat the warp's filter (T, then the
+//     K-th entry of the warp's running list) enter that list; the warps'
+//     lists merge into the row's top K.  K = 1 needs one pass: each thread's
+//     argmax.
+// (registers capped for six CTAs per SM, eight for the one-pass K = 1)
 template <int K>
-__global__ void __launch_bounds__(kThreads) softmax_topk_kernel(const float* __restrict__ x,
-                                                                int64_t cols, int nct, int vec,
-                                                                int k, int32_t* __restrict__ idx,
-                                                                float* __restrict__ prob) {
+__global__ void __launch_bounds__(kThreads, K > 1 ? 6 : 8)
+    softmax_topk_kernel(const float* __restrict__ x, int64_t cols, int nct, int vec, int k,
+                        int32_t* __restrict__ idx, float* __restrict__ prob) {
   __shared__ float s_pv[kWarps * 32];  // the warps' sorted lists
   __shared__ int s_pi[kWarps * 32];
   __shared__ float s_m[kWarps], s_l[kWarps];
   __shared__ float c_v[32];  // this CTA's list and summary, read by CTA 0 of the cluster
   __shared__ int c_i[32];
   __shared__ float c_ml[2];
+  __shared__ float s_gm[(K > 1 ? kGroupSlots : 1) * kThreads];  // K > 1: the group maxima
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_ctarank();
@@ -330,16 +367,32 @@ __global__ void __launch_bounds__(kThreads) softmax_topk_kernel(const float* __r
       l += (ptx::ex2((v.x - m) * kLog2e) + ptx::ex2((v.y - m) * kLog2e)) +
            (ptx::ex2((v.z - m) * kLog2e) + ptx::ex2((v.w - m) * kLog2e));
   };
+  // group g of this thread: float4s f0 + tid + 4 * kThreads * g + kThreads * u, u < 4
+  auto note_group = [&](int g, float gx) {
+    if constexpr (K > 1) {
+      float* p = &s_gm[(g & (kGroupSlots - 1)) * kThreads + tid];
+      *p = g < kGroupSlots ? gx : fmaxf(*p, gx);
+    }
+  };
   if (vec) {
     int64_t f = f0 + tid;
-    for (; f + 3 * kThreads < f1; f += 4 * kThreads) {  // four 16-byte loads in flight
+    int g = 0;
+    for (; f + 3 * kThreads < f1; f += 4 * kThreads, ++g) {  // four 16-byte loads in flight
       const float4 a = x4[f], b = x4[f + kThreads];
       const float4 c = x4[f + 2 * kThreads], d = x4[f + 3 * kThreads];
       {  // the 16 entries' maximum, one rescale of l, 16 terms: one basic block
         const float4 e[4] = {a, b, c, d};
         float mg = m;
+        if constexpr (K > 1) {  // the group's own maximum is kept for the second pass
+          float gx = fmaxf(fmaxf(e[0].x, e[0].y), fmaxf(e[0].z, e[0].w));
 #pragma unroll
-        for (int u = 0; u < 4; ++u) mg = fmaxf(mg, fmaxf(fmaxf(e[u].x, e[u].y), fmaxf(e[u].z, e[u].w)));
+          for (int u = 1; u < 4; ++u) gx = fmaxf(gx, fmaxf(fmaxf(e[u].x, e[u].y), fmaxf(e[u].z, e[u].w)));
+          note_group(g, gx);
+          mg = fmaxf(m, gx);
+        } else {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) mg = fmaxf(mg, fmaxf(fmaxf(e[u].x, e[u].y), fmaxf(e[u].z, e[u].w)));
+        }
         float s = l * ptx::ex2((m - mg) * kLog2e);
 #pragma unroll
         for (int u = 0; u < 4; ++u)
@@ -360,15 +413,18 @@ __global__ void __launch_bounds__(kThreads) softmax_topk_kernel(const float* __r
         }
       }
     }
+    float gt = kNegInf;  // the last (partial, possibly empty) group
     for (; f < f1; f += kThreads) {
       const float4 a = x4[f];
       add4(a);
+      gt = fmaxf(gt, fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)));
       const int j = static_cast<int>(4 * f);
       best(a.x, j);
       best(a.y, j + 1);
       best(a.z, j + 2);
       best(a.w, j + 3);
     }
+    note_group(g, gt);
   } else {
     for (int64_t j = c0 + tid; j < c1; j += kThreads) {
       const float a = xr[j];
@@ -438,17 +494,8 @@ __global__ void __launch_bounds__(kThreads) softmax_topk_kernel(const float* __r
     __syncthreads();
     thr = fmaxf(thr, c_ml[0]);
   }
-  __syncthreads();
-  if (tid == 0) {  // the CTA's (m, l), read by CTA 0 at the end
-    float M = s_m[0], Ls = s_l[0];
-    for (int w = 1; w < kWarps; ++w) {
-      const float mn = fmaxf(M, s_m[w]);
-      Ls = Ls * rebase(M, mn) + s_l[w] * rebase(s_m[w], mn);
-      M = mn;
-    }
-    c_ml[0] = M;
-    c_ml[1] = Ls;
-  }
+  // no CTA barrier here: each warp's second pass needs only its own filter
+  // (the CTA's (m, l) is merged after the lists' first barrier)
 
   // ---- pass 2: entries that beat the filter enter the warp's running best 32
   // (lane-sorted).  The filter starts at (thr, any index) and tightens to the
@@ -457,12 +504,24 @@ __global__ void __launch_bounds__(kThreads) softmax_topk_kernel(const float* __r
   {
     float kv = thr;
     int ki = kNoIndex;
-    // The lanes' candidates enter the list one at a time: each is broadcast,
-    // its place is the first lane whose entry it comes before, and the lanes
-    // from there on shift up by one (the last entry drops out).  Candidates
-    // are few after the threshold, so this beats sorting each batch.
+    // A round's candidates (at most one per lane) enter the list one at a
+    // time when they are few: each is broadcast, its place is the first lane
+    // whose entry it comes before, and the lanes from there on shift up by one
+    // (the last entry drops out).  More than eight (a row with many equal
+    // maxima, say) are sorted as a batch and merged into the list instead.
     auto round = [&](float cv, int ci) {
       unsigned cl = __ballot_sync(0xffffffffu, ci != kNoIndex);
+      if (__popc(cl) > 8) {  // many at once: sort them and merge the batch
+        warp_sort_pairs(cv, ci);
+        warp_merge_pairs(v0, i0, cv, ci);
+        const float nv = __shfl_sync(0xffffffffu, v0, K - 1);
+        const int ni = __shfl_sync(0xffffffffu, i0, K - 1);
+        if (ni != kNoIndex && before(nv, ni, kv, ki)) {
+          kv = nv;
+          ki = ni;
+        }
+        return;
+      }
       while (cl) {
         const int src = __ffs(cl) - 1;
         cl &= cl - 1;
@@ -491,53 +550,93 @@ __global__ void __launch_bounds__(kThreads) softmax_topk_kernel(const float* __r
     };
     v0 = kNegInf;
     i0 = kNoIndex;
-    if (vec) {
-      for (int64_t f = f0 + tid; f - tid < f1; f += 4 * kThreads) {
-        float4 a[4];
+    // The entries of the group at float4 f (when on) that beat the filter are
+    // offered to the list, one per lane per round.
+    auto offer = [&](int64_t f, bool on) {
+      float4 a[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          a[u] = f + u * kThreads < f1 ? __ldcs(x4 + f + u * kThreads)
-                                       : make_float4(kNegInf, kNegInf, kNegInf, kNegInf);
-        uint32_t msk = 0;
+      for (int u = 0; u < 4; ++u)
+        a[u] = on && f + u * kThreads < f1 ? __ldcs(x4 + f + u * kThreads)
+                                           : make_float4(kNegInf, kNegInf, kNegInf, kNegInf);
+      uint32_t msk = 0;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          // past the slice: no entry.  Selects instead of a branch measured
-          // 2-5 % faster for k <= 16 and 10 % slower at k = 32.
-          if constexpr (K <= 16) {
-            const uint32_t b = (a[u].x >= kv ? 1u : 0u) | (a[u].y >= kv ? 2u : 0u) |
-                               (a[u].z >= kv ? 4u : 0u) | (a[u].w >= kv ? 8u : 0u);
-            msk |= (f + u * kThreads < f1 ? b : 0u) << (4 * u);
-          } else {
-            if (f + u * kThreads >= f1) continue;
-            msk |= (a[u].x >= kv ? 1u : 0u) << (4 * u);
-            msk |= (a[u].y >= kv ? 2u : 0u) << (4 * u);
-            msk |= (a[u].z >= kv ? 4u : 0u) << (4 * u);
-            msk |= (a[u].w >= kv ? 8u : 0u) << (4 * u);
+      for (int u = 0; u < 4; ++u) {
+        // past the slice: no entry.  Selects instead of a branch measured
+        // 2-5 % faster for k <= 16 and 10 % slower at k = 32.
+        const bool in = on && f + u * kThreads < f1;
+        if constexpr (K <= 16) {
+          const uint32_t b = (a[u].x >= kv ? 1u : 0u) | (a[u].y >= kv ? 2u : 0u) |
+                             (a[u].z >= kv ? 4u : 0u) | (a[u].w >= kv ? 8u : 0u);
+          msk |= (in ? b : 0u) << (4 * u);
+        } else {
+          if (!in) continue;
+          msk |= (a[u].x >= kv ? 1u : 0u) << (4 * u);
+          msk |= (a[u].y >= kv ? 2u : 0u) << (4 * u);
+          msk |= (a[u].z >= kv ? 4u : 0u) << (4 * u);
+          msk |= (a[u].w >= kv ? 8u : 0u) << (4 * u);
+        }
+      }
+      while (__any_sync(0xffffffffu, msk != 0)) {
+        float cv = kNegInf;
+        int ci = kNoIndex;
+        while (msk) {  // this lane's next entry that still beats the filter
+          const int e = __ffs(msk) - 1;
+          msk &= msk - 1;
+          const int u = e >> 2, c = e & 3;
+          float4 w = a[0];
+          if (u == 1) w = a[1];
+          if (u == 2) w = a[2];
+          if (u == 3) w = a[3];
+          float v = w.x;
+          if (c == 1) v = w.y;
+          if (c == 2) v = w.z;
+          if (c == 3) v = w.w;
+          const int j = static_cast<int>(4 * (f + u * kThreads)) + c;
+          if (before(v, j, kv, ki)) {
+            cv = v;
+            ci = j;
+            break;
           }
         }
-        while (__any_sync(0xffffffffu, msk != 0)) {
-          float cv = kNegInf;
-          int ci = kNoIndex;
-          while (msk) {  // this lane's next entry that still beats the filter
-            const int e = __ffs(msk) - 1;
-            msk &= msk - 1;
-            const int u = e >> 2, c = e & 3;
-            float4 w = a[0];
-            if (u == 1) w = a[1];
-            if (u == 2) w = a[2];
-            if (u == 3) w = a[3];
-            float v = w.x;
-            if (c == 1) v = w.y;
-            if (c == 2) v = w.z;
-            if (c == 3) v = w.w;
-            const int j = static_cast<int>(4 * (f + u * kThreads)) + c;
-            if (before(v, j, kv, ki)) {
-              cv = v;
-              ci = j;
-              break;
-            }
+        round(cv, ci);
+      }
+    };
+    if (vec) {
+      // Only groups whose maximum reaches thr can hold a candidate.  The warp
+      // lists its (lane, slot) pairs that do and shares them out, one per lane
+      // per batch of 32, so a warp re-reads a few groups instead of its slice.
+      const int ng = static_cast<int>((f1 - f0 + 4 * kThreads - 1) / (4 * kThreads));
+      const int nslots = ng < kGroupSlots ? ng : kGroupSlots;
+      unsigned my_pm = 0;  // lane s: the lanes whose slot-s groups reach thr
+      for (int s = 0; s < nslots; ++s) {
+        const unsigned pm = __ballot_sync(0xffffffffu, s_gm[s * kThreads + tid] >= thr);
+        if (lane == s) my_pm = pm;
+      }
+      int incl = __popc(my_pm);  // pairs in slots 0..lane
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      const int total = __shfl_sync(0xffffffffu, incl, 31);
+      const int trips = (ng + kGroupSlots - 1) / kGroupSlots;  // groups per slot, at most
+      for (int t0 = 0; t0 < total; t0 += 32) {
+        const int t = t0 + lane;  // this lane's pair
+        int slot = 0, skip = 0;   // its slot, and the pairs in the slots before it
+        for (int s2 = 0; s2 < nslots; ++s2) {
+          const int is = __shfl_sync(0xffffffffu, incl, s2);
+          if (is <= t) {
+            slot = s2 + 1;
+            skip = is;
           }
-          round(cv, ci);
+        }
+        const bool task = t < total;
+        const unsigned pm = __shfl_sync(0xffffffffu, my_pm, slot & 31);
+        const int src = task ? nth_set_bit(pm, t - skip) : 0;
+        const int64_t fb = f0 + warp * 32 + src;
+        for (int r = 0; r < trips; ++r) {
+          const int gg = slot + r * kGroupSlots;
+          offer(fb + static_cast<int64_t>(4 * kThreads) * gg, task && gg < ng);
         }
       }
     } else {
@@ -554,7 +653,7 @@ __global__ void __launch_bounds__(kThreads) softmax_topk_kernel(const float* __r
   if constexpr (K == 1) {
     cluster_topk<K>(L, s_pv, s_pi, c_v, c_i, nct, rank, v0, i0);
   } else {
-    cluster_merge_lists(v0, i0, s_pv, s_pi, c_v, c_i, nct, rank);
+    cluster_merge_lists(v0, i0, s_pv, s_pi, s_m, s_l, c_ml, c_v, c_i, nct, rank);
   }
   if (rank == 0 && warp == 0) {
     // the row's (M, L), merged in rank order

@@ -93,6 +93,29 @@ def test_cluster_split_rows(cuda_ok):
     assert int(idx[1, 0]) == (1 << 20) - 1
 
 
+def test_group_filter_edge_rows(cuda_ok):
+    """The second pass reads again only the groups of 16 entries whose maximum
+    reaches the warp's threshold.  Rows where most groups do (heavy ties, all
+    equal), where a thread's groups share a slot (slices longer than 16 steps
+    of the first pass), where the few finite entries are spread over those
+    shared slots, and where the best entries sit in the ragged last group of
+    the last slice."""
+    cols = (1 << 20) + 12
+    rng = np.random.default_rng(76)
+    x = rng.integers(-4, 5, size=(4, cols)).astype(np.float32)   # ties: most groups hold a 4
+    x[1, :] = -np.inf
+    x[1, rng.choice(cols, 40, replace=False)] = rng.normal(size=40).astype(np.float32)
+    x[2, :] = 0.5                                                 # all equal
+    x[3] = rng.normal(size=cols).astype(np.float32)
+    x[3, cols - 3:] = [50.0, 60.0, 70.0]
+    xt = torch.from_numpy(x)
+    for k in (2, 8, 32):
+        idx, prob = osm.softmax_topk(xt.cuda(), k)
+        check(xt, k, idx, prob)
+        assert torch.equal(idx[2].cpu(), torch.arange(k, dtype=torch.int32))
+        assert idx[3, 0] == cols - 1 and idx[3, 1] == cols - 2
+
+
 def test_full_size_rows(cuda_ok):
     """4096 x 32768 softmax workload (2 N(0,1), 1% of entries = 40.0), k = 8:
     every row's indices exactly, probabilities within the bar."""
