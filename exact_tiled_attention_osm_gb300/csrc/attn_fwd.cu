@@ -36,9 +36,13 @@
 //              TMEM -> registers, mask, scale and subtract the reference in
 //              packed f32x2, independent exp2 (so the MUFU latency is
 //              covered), row sum, bf16 pack, store P over the S columns
-//              already consumed; epilogue O = O~ / l (staged per warp in
-//              shared memory so that global stores cover whole 64-byte row
-//              segments), lse.
+//              already consumed; epilogue: the row's O~ in one TMEM load
+//              (which frees the region for the next item at once),
+//              O = O~ / l in bf16 through a per-warp shared-memory stage
+//              that the tensor-memory engine stores (bulk tensor stores of
+//              32 x 64 boxes), lse.  A warp takes its next work item before
+//              it waits for O, so the queue and key_len reads stay off the
+//              next item's first tile.
 //   TMEM       512 columns: S_0 | S_1 | O~_0 | O~_1 (128 fp32 columns each).
 // The reference subtracted before exp2 need not be the running maximum: every
 // identity of the recurrence holds for any common reference ("Precision, and
@@ -105,13 +109,11 @@ enum Bar : uint32_t {
 constexpr uint32_t kSmemTmemSlot = kSmemBar + 8 * NUM_BARS;
 constexpr uint32_t kSmemAbort = kSmemTmemSlot + 4;
 constexpr uint32_t kSmemItems = kSmemAbort + 4;  // int[kItemSlots]: the CTA's item queue
-// per softmax warp: one 32-column chunk of its 32 output rows (bf16), staged
-// so that the warp's global stores cover whole 64-byte row segments
-constexpr uint32_t kStageBytes = 32 * 64;
-constexpr uint32_t kSmemStage = (kSmemItems + 4 * kItemSlots + 127) / 128 * 128;
-// two stages per softmax warp, in turn, so a chunk's box need not have left
-// the stage before the next chunk is written
-constexpr uint32_t kSmemBytes = kSmemStage + 2 * 8 * kStageBytes + 1024;  // + alignment slack
+// per softmax warp: a 64-column half of its 32 output rows (bf16, 128 bytes
+// a row, in the 128-byte swizzle of the output's tensor map), 1024-aligned
+constexpr uint32_t kStageBytes = 32 * 128;
+constexpr uint32_t kSmemStage = (kSmemItems + 4 * kItemSlots + 1023) / 1024 * 1024;
+constexpr uint32_t kSmemBytes = kSmemStage + 8 * kStageBytes + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 // readers of the item queue: the MMA thread and the eight softmax warps
 constexpr uint32_t kItemReaders = 1 + 8;
@@ -128,6 +130,20 @@ constexpr unsigned kSite = 0x01000000u;
 constexpr unsigned kChk = 0x0E010000u;
 
 
+// A row's whole O~ (D fp32 columns) from TMEM in one load, the wait inside
+// the same asm statement.
+__device__ __forceinline__ void tmem_ld_x128(uint32_t taddr, uint32_t (&r)[128]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, %96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%128];\n"
+               "tcgen05.wait::ld.sync.aligned;\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+               : "r"(taddr) : "memory");
+}
+template <int D>
+__device__ __forceinline__ void tmem_ld_row(uint32_t taddr, uint32_t (&r)[D]) {
+  if constexpr (D == 128) tmem_ld_x128(taddr, r);
+  else tmem_ld_x64(taddr, r);
+}
+
 // Store a 3-D box from shared memory (row-major, no swizzle) to global memory
 // through the tensor map, as one bulk group; rows outside the tensor are not
 // written.  The caller waits (bulk_wait_read) before it rewrites the source.
@@ -139,10 +155,9 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
       "r"(src), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
-// every bulk store this thread issued, except the most recent one, has read
-// its shared-memory source
-__device__ __forceinline__ void bulk_wait_read_1() {
-  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+// every bulk store this thread issued has read its shared-memory source
+__device__ __forceinline__ void bulk_wait_read_0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 // every bulk store this thread issued has completed
 __device__ __forceinline__ void bulk_wait_all() {
@@ -492,14 +507,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     uint32_t sf_ph = 0, of_ph = 0;
     bool ok = true;
-    while (ok) {
-      if (!(ok = wait_all(bar(ITEM_FULL + iq_slot), iq_ph, kSite | 11))) break;
+    // The next work item from the CTA's queue (-1: none left, -2: the bounded
+    // wait gave up) and what it covers.  A warp takes it before it waits for
+    // the current item's output, so that the wait and the epilogue, not the
+    // next item's first tile, absorb the queue and key_len reads.
+    Item nit{};
+    auto take_item = [&]() -> int {
+      if (!wait_all(bar(ITEM_FULL + iq_slot), iq_ph, kSite | 11)) return -2;
       const int item = item_q[iq_slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(ITEM_EMPTY + iq_slot));
       iq_advance();
-      if (item < 0) break;
-      const Item it = item_info(p, item);
+      if (item >= 0) nit = item_info(p, item);
+      return item;
+    };
+    int next = take_item();
+    while (next >= 0) {
+      const Item it = nit;
       const int row = it.q0 + t * kRows + 32 * wq + lane;
       const bool row_ok = row < p.Nq;
       const int64_t orow = static_cast<int64_t>(it.bh) * p.Nq + row;
@@ -511,6 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
           p.lse[orow] = kNegInf;
         }
+        next = take_item();
         continue;
       }
       int limit = it.kv_len;
@@ -755,48 +780,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         l += (la[0] + la[1]) + (la[2] + la[3]);
       }
       if (!ok) break;
+      next = take_item();
       ok = wait_all(bar(O_FULL + t), of_ph, kSite | 8);
       if (!ok) break;
       of_ph ^= 1;
       tc_fence_after();
       const float inv = kNorm ? (l > 0.f ? 1.f : 0.f) : (l + corr > 0.f ? 1.f / (l + corr) : 0.f);
-      // O = O~ / l in bf16, a 32-column chunk at a time: each thread puts its
-      // row's 64 bytes into the warp's staging area (32 rows x 64 bytes,
-      // row-major), and one lane hands the 32 x 32 box to the tensor-memory
-      // engine as a bulk store (rows past Nq are not written), so the warp
-      // does not wait for its global stores
-      // (formed from the shared array itself, so the stage writes are
-      // shared-memory stores)
-      uint8_t* stage_base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u) +
-                            kSmemStage + (warp - 4) * 2 * kStageBytes;
+      // O = O~ / l in bf16, a 64-column half at a time: each thread puts its
+      // row's 128 bytes into the warp's stage (32 rows x 128 bytes, 16-byte
+      // pieces in the 128-byte swizzle, so the lanes' writes meet no bank
+      // twice), and one lane hands the 32 x 64 box to the tensor-memory engine
+      // as a bulk store (rows past Nq are not written), so the warp does not
+      // wait for its global stores.  (The stage is formed from the shared
+      // array itself, so its writes are shared-memory stores.)
+      uint8_t* stage = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u) + kSmemStage +
+                       (warp - 4) * kStageBytes;
+      const uint32_t stage_s = smem_u32(stage);
+      uint4* srow = reinterpret_cast<uint4*>(stage + 128 * lane);
       const int row0 = row - lane;  // the warp's first row in its head
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint4* stage = reinterpret_cast<uint4*>(stage_base + (c & 1) * kStageBytes);
-        const uint32_t stage_s = smem_u32(stage);
-        uint32_t orr[32];
-        tmem_ld_x32(tO + 32 * c, orr);
-        uint32_t pk2[16];
+      // the row's whole O~ in one TMEM load, so the region is free for the
+      // next item's products before the conversions and stores
+      uint32_t orr[D];
+      tmem_ld_row<D>(tO, orr);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(O_EMPTY + t));
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(orr[2 * e]) * inv,
-                                                    __uint_as_float(orr[2 * e + 1]) * inv);
+      for (int h = 0; h < D / 64; ++h) {
+        uint32_t pk2[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(orr[64 * h + 2 * e]) * inv,
+                                                    __uint_as_float(orr[64 * h + 2 * e + 1]) * inv);
           pk2[e] = *reinterpret_cast<uint32_t*>(&h2);
         }
-        if (lane == 0) bulk_wait_read_1();  // the box written two chunks ago has left this stage
+        if (lane == 0) bulk_wait_read_0();  // the previous box has left the stage
         __syncwarp();
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          stage[lane * 4 + e] = make_uint4(pk2[4 * e], pk2[4 * e + 1], pk2[4 * e + 2], pk2[4 * e + 3]);
+        for (int e = 0; e < 8; ++e)
+          srow[e ^ (lane & 7)] = make_uint4(pk2[4 * e], pk2[4 * e + 1], pk2[4 * e + 2], pk2[4 * e + 3]);
         fence_proxy_async_smem();
         __syncwarp();
         // (a warp whose rows all lie past Nq stores nothing)
         if (lane == 0 && row0 < p.Nq && checked(it.bh < p.B * p.H && row0 >= 0, p.err, kChk | 4))
-          tma_store_3d(&tm_o, stage_s, 32 * c, row0, it.bh);
+          tma_store_3d(&tm_o, stage_s, 64 * h, row0, it.bh);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(O_EMPTY + t));
       if (row_ok && checked(orow < n_rows, p.err, kChk | 5))
         p.lse[orow] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : kNegInf;
     }
@@ -857,7 +885,7 @@ cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o
   if (!make_tmap_bf16_3d(&tq, q, d, Nq, BH, 64, kRows) ||
       !make_tmap_bf16_3d(&tk, k, d, Nk, BH, 64, kKeys) ||
       !make_tmap_bf16_3d(&tv, v, d, Nk, BH, 64, kKeys) ||
-      !make_tmap_bf16_3d(&to, o, d, Nq, BH, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE)) {
+      !make_tmap_bf16_3d(&to, o, d, Nq, BH, 64, 32)) {
     *tmap_ok = false;
     return cudaSuccess;
   }
