@@ -25,8 +25,8 @@
 //                     and dK += dS^T Q read them straight from TMEM.
 // dQ and dK/dV are separate so that no partial sum crosses CTAs (no atomics);
 // the price is S and dP formed twice (7 instead of 5 matrix products).  The
-// outputs leave through a per-warp shared-memory stage so that every store
-// covers whole 64-byte row segments.
+// outputs leave through bulk tensor stores of boxes that each warp stages in
+// the ring's shared memory, idle once the last product has completed.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -81,11 +81,10 @@ constexpr uint32_t kSmemAbort = kSmemTmemSlot + 4;
 // per softmax warp: [2 buffers][lse2 | D][128 columns] floats
 constexpr uint32_t kSmemCol = (kSmemAbort + 4 + 15) / 16 * 16;
 constexpr uint32_t kColFloats = 2 * 2 * (kTile / 2);
-// per element-wise warp: one 32-column chunk of its 32 output rows (bf16),
-// staged so that the warp's global stores cover whole 64-byte row segments
-constexpr uint32_t kStageBytes = 32 * 64;
-constexpr uint32_t kSmemStage = (kSmemCol + 8 * kColFloats * 4 + 127) / 128 * 128;
-constexpr uint32_t kSmemBytes = kSmemStage + 8 * kStageBytes + 1024;
+// The outputs leave through the ring, idle once every product has completed:
+// each element-wise warp stages its 32 rows there (at most 8 KB) for bulk
+// tensor stores.
+constexpr uint32_t kSmemBytes = kSmemCol + 8 * kColFloats * 4 + 1024;  // + alignment slack
 
 constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemAcc0 = 256, kTmemAcc1 = 384;
 
@@ -118,39 +117,45 @@ __host__ __device__ constexpr uint32_t tmem_half_col(int kk) {
   return static_cast<uint32_t>(64 * (kk >> 2) + 8 * (kk & 3));
 }
 
-// The warp's 32 rows of a bf16 output (row r at base + r * D), 32-column
-// chunks c0 .. c1-1 read from TMEM and scaled by mul: each thread puts its
-// row's 64 bytes of a chunk into the warp's staging area, then the warp stores
-// 8 rows x 64 contiguous bytes per instruction.  Rows from nvalid on are not
-// stored.
-template <int D>
-__device__ __forceinline__ void store_rows_bf16_staged(uint32_t t_acc, float mul,
-                                                       __nv_bfloat16* base, int nvalid, int c0,
-                                                       int c1, uint4* stage) {
+// A warp's 32 accumulator rows (this thread's row in r, N fp32 columns, times
+// mul) as bf16 in a shared-memory stage laid out for bulk tensor stores:
+// N / 64 boxes of 32 rows x 64 columns (4 KB each), 128 bytes a row, the
+// 16-byte pieces in the 128-byte swizzle (piece e of row r at e ^ (r & 7)),
+// so the lanes' writes meet no bank twice.  The stage is 1024-byte aligned.
+template <int N>
+__device__ __forceinline__ void stage_rows_sw128(const uint32_t (&r)[N], float mul, uint8_t* stage) {
   const int lane = threadIdx.x & 31;
-#pragma unroll 1
-  for (int c = c0; c < c1; ++c) {
-    uint32_t r[32];
-    tmem_ld_x32(t_acc + 32 * c, r);
-    uint32_t pk[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(r[2 * e]) * mul,
-                                                __uint_as_float(r[2 * e + 1]) * mul);
-      pk[e] = *reinterpret_cast<uint32_t*>(&h2);
+  for (int h = 0; h < N / 64; ++h) {
+    uint4* srow = reinterpret_cast<uint4*>(stage + 4096 * h + 128 * lane);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      uint32_t w[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(r[64 * h + 8 * e + 2 * u]) * mul,
+                                                  __uint_as_float(r[64 * h + 8 * e + 2 * u + 1]) * mul);
+        w[u] = *reinterpret_cast<uint32_t*>(&h2);
+      }
+      srow[e ^ (lane & 7)] = make_uint4(w[0], w[1], w[2], w[3]);
     }
+  }
+}
+// The same for 32 columns: one box of 32 rows x 32 columns, 64 bytes a row,
+// no swizzle.
+__device__ __forceinline__ void stage_rows_32(const uint32_t (&r)[32], float mul, uint8_t* stage) {
+  const int lane = threadIdx.x & 31;
+  uint4* srow = reinterpret_cast<uint4*>(stage + 64 * lane);
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      stage[lane * 4 + e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-    __syncwarp();
+  for (int e = 0; e < 4; ++e) {
+    uint32_t w[4];
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      const int rr = 8 * g + (lane >> 2);
-      if (rr < nvalid)
-        reinterpret_cast<uint4*>(base + static_cast<int64_t>(rr) * D + 32 * c)[lane & 3] =
-            stage[rr * 4 + (lane & 3)];
+    for (int u = 0; u < 4; ++u) {
+      __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(r[8 * e + 2 * u]) * mul,
+                                                __uint_as_float(r[8 * e + 2 * u + 1]) * mul);
+      w[u] = *reinterpret_cast<uint32_t*>(&h2);
     }
-    __syncwarp();
+    srow[e] = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -195,7 +200,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const Params p) {
+                  const __grid_constant__ CUtensorMap tm_dq, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned by pointer arithmetic on the shared array, so that
   // accesses through it compile to shared-memory instructions (an integer
@@ -469,14 +474,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       tc_fence_after();
       const int row0 = row - lane;  // the warp's first query row
-      // the rows written: [row0, row0 + min(32, Nq - row0)), none when the
-      // warp's rows all lie past Nq
-      if (checked(bh < p.B * p.H && row0 >= 0, p.err, kChk | 2))
-        store_rows_bf16_staged<D>(
-            tbase + lane_off + kTmemAcc0, p.scale,
-            p.dq + (static_cast<int64_t>(bh) * p.Nq + row0) * D, min(32, p.Nq - row0),
-            hh * (D / 64), (hh + 1) * (D / 64),
-            reinterpret_cast<uint4*>(smem + kSmemStage + (warp - 4) * kStageBytes));
+      // this warp's half of its rows' dQ (D / 2 columns) staged in the idle
+      // ring and stored as one box; rows past Nq are not written, and a warp
+      // whose rows all lie past Nq stores nothing
+      constexpr int kHalf = D / 2;
+      uint8_t* stage = smem + kSmemRing + (warp - 4) * (32 * kHalf * 2);
+      uint32_t r[kHalf];
+      tmem_ld_cols<kHalf>(tbase + lane_off + kTmemAcc0 + hh * kHalf, r);
+      if constexpr (kHalf == 64) stage_rows_sw128<kHalf>(r, p.scale, stage);
+      else stage_rows_32(r, p.scale, stage);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && row0 < p.Nq && checked(bh < p.B * p.H && row0 >= 0, p.err, kChk | 2)) {
+        tma_store_3d(&tm_dq, smem_u32(stage), hh * kHalf, row0, bh);
+        bulk_wait_read_0();  // the box has left shared memory before the CTA ends
+      }
     }
   }
   tc_fence_before();
@@ -492,7 +504,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
-                    const __grid_constant__ CUtensorMap tm_do, const Params p) {
+                    const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dk,
+                    const __grid_constant__ CUtensorMap tm_dv, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned by pointer arithmetic on the shared array, so that
   // accesses through it compile to shared-memory instructions (an integer
@@ -811,15 +824,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       tc_fence_after();
       const int key0 = key - lane;  // the warp's first key row
-      const int64_t g = (static_cast<int64_t>(bh) * p.Nk + key0) * D;
-      uint4* stage = reinterpret_cast<uint4*>(smem + kSmemStage + (warp - 4) * kStageBytes);
-      if (!checked(bh < p.B * p.H && key0 >= 0, p.err, kChk | 4)) {  // rows as for dQ
-      } else if (hh == 0)
-        store_rows_bf16_staged<D>(tbase + lane_off + kTmemAcc0, 1.f, p.dv + g,
-                                  min(32, p.Nk - key0), 0, D / 32, stage);
-      else
-        store_rows_bf16_staged<D>(tbase + lane_off + kTmemAcc1, p.scale, p.dk + g,
-                                  min(32, p.Nk - key0), 0, D / 32, stage);
+      // this warp's rows of dV (hh = 0) or dK (hh = 1) staged in the idle
+      // ring and stored as D / 64 boxes; rows past Nk are not written
+      uint8_t* stage = smem + kSmemRing + (warp - 4) * (32 * D * 2);
+      uint32_t r[D];
+      tmem_ld_row<D>(tbase + lane_off + (hh == 0 ? kTmemAcc0 : kTmemAcc1), r);
+      stage_rows_sw128<D>(r, hh == 0 ? 1.f : p.scale, stage);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && key0 < p.Nk && checked(bh < p.B * p.H && key0 >= 0, p.err, kChk | 4)) {
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h)
+          tma_store_3d(hh == 0 ? &tm_dv : &tm_dk, smem_u32(stage) + 4096 * h, 64 * h, key0, bh);
+        bulk_wait_read_0();  // the boxes have left shared memory before the CTA ends
+      }
     }
   }
   tc_fence_before();
@@ -857,11 +875,17 @@ cudaError_t launch_attn_bwd(const void* q, const void* k, const void* v, const v
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
+  // outputs: boxes of 32 rows x 64 columns in the 128-byte swizzle; dQ at
+  // d = 64 goes out as 32 x 32 halves without swizzle
   if (!make_tmap_bf16_3d(&tq, q, d, Nq, BH, 64, kTile) ||
       !make_tmap_bf16_3d(&tk, k, d, Nk, BH, 64, kTile) ||
       !make_tmap_bf16_3d(&tv, v, d, Nk, BH, 64, kTile) ||
-      !make_tmap_bf16_3d(&tdo, dout, d, Nq, BH, 64, kTile)) {
+      !make_tmap_bf16_3d(&tdo, dout, d, Nq, BH, 64, kTile) ||
+      !make_tmap_bf16_3d(&tdk, dk, d, Nk, BH, 64, 32) ||
+      !make_tmap_bf16_3d(&tdv, dv, d, Nk, BH, 64, 32) ||
+      !(d == 128 ? make_tmap_bf16_3d(&tdq, dq, d, Nq, BH, 64, 32)
+                 : make_tmap_bf16_3d(&tdq, dq, d, Nq, BH, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE))) {
     *tmap_ok = false;
     return cudaSuccess;
   }
@@ -905,9 +929,9 @@ cudaError_t launch_attn_bwd(const void* q, const void* k, const void* v, const v
   if (Nk > 0 && Nq > 0) {
     const unsigned g = static_cast<unsigned>(BH * p.n_kt);
     if (d == 128)
-      bwd_dkdv_kernel<128><<<g, kThreads, kSmemBytes, s>>>(tq, tk, tv, tdo, p);
+      bwd_dkdv_kernel<128><<<g, kThreads, kSmemBytes, s>>>(tq, tk, tv, tdo, tdk, tdv, p);
     else
-      bwd_dkdv_kernel<64><<<g, kThreads, kSmemBytes, s>>>(tq, tk, tv, tdo, p);
+      bwd_dkdv_kernel<64><<<g, kThreads, kSmemBytes, s>>>(tq, tk, tv, tdo, tdk, tdv, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   } else if (Nk > 0) {  // no query: dK = dV = 0
@@ -919,9 +943,9 @@ cudaError_t launch_attn_bwd(const void* q, const void* k, const void* v, const v
     if (Nk > 0) {
       const unsigned g = static_cast<unsigned>(BH * p.n_qt);
       if (d == 128)
-        bwd_dq_kernel<128><<<g, kThreads, kSmemBytes, s>>>(tq, tk, tv, tdo, p);
+        bwd_dq_kernel<128><<<g, kThreads, kSmemBytes, s>>>(tq, tk, tv, tdo, tdq, p);
       else
-        bwd_dq_kernel<64><<<g, kThreads, kSmemBytes, s>>>(tq, tk, tv, tdo, p);
+        bwd_dq_kernel<64><<<g, kThreads, kSmemBytes, s>>>(tq, tk, tv, tdo, tdq, p);
       e = cudaGetLastError();
     } else {  // no key: dQ = 0
       e = cudaMemsetAsync(dq, 0, static_cast<size_t>(BH) * Nq * d * 2, s);
