@@ -45,20 +45,20 @@ CSRC = os.path.join(ROOT, "exact_tiled_attention_osm_gb300", "csrc")
 # operation), valid only for the kernel sources it was captured on (sha256 of
 # the listed files, concatenated); None until captured on the current source.
 KERNEL_TRAFFIC = {
-    # attn_fwd_kernel<false, 128>, causal+padding B8 H32 N8192: read 1,333,773,568
-    # + write 519,139,584
-    "attn_fwd_kernel": {"bytes_per_launch": 1_333_773_568 + 519_139_584,
+    # attn_fwd_kernel<false, 128>, causal+padding B8 H32 N8192: read 1,335,807,744
+    # + write 519,688,192
+    "attn_fwd_kernel": {"bytes_per_launch": 1_335_807_744 + 519_688_192,
                         "sources": ["attn_fwd.cu", "ptx.cuh"],
-                        "source_sha256": "4a521ca9af642e7dd271d55915389a452132c2145b45d96acd457faa7a6c47e3"},
-    # softmax_rows_cluster<8>, 4096 x 32768: read 536,902,144 + write 482,932,736
-    "softmax_rows": {"bytes_per_launch": 536_902_144 + 482_932_736,
+                        "source_sha256": "6ff9ae89e7ceca73af8091b19a4c919b3cc91c9db1e7abea1253f029c687dceb"},
+    # softmax_rows_cluster<8>, 4096 x 32768: read 536,921,088 + write 482,430,208
+    "softmax_rows": {"bytes_per_launch": 536_921_088 + 482_430_208,
                      "sources": ["softmax_rows.cu", "exp_le0.cuh", "ptx.cuh"],
-                     "source_sha256": "75f64fc7cf44844ecc1954fa06f9f15d46c1e80fc56aa2f001e6655e385b4a6e"},
-    # decode_split_kernel read 17,360,707,328 + write 11,661,312;
-    # merge_kernel read 17,050,368 + write 0
-    "decode_splitkv": {"bytes_per_launch": 17_360_707_328 + 11_661_312 + 17_050_368,
+                     "source_sha256": "c84597e1141cf857b1bb5c183ced97a033a0280f8a9e4888cdb55ade18b7b39e"},
+    # decode_split_kernel read 17,360,717,824 + write 11,526,144;
+    # merge_kernel read 17,050,880 + write 0
+    "decode_splitkv": {"bytes_per_launch": 17_360_717_824 + 11_526_144 + 17_050_880,
                        "sources": ["decode.cu", "ptx.cuh"],
-                       "source_sha256": "2c4a67054d27031ea9697220946b0f37ca58359852568d502f2e77ad0c255509"},
+                       "source_sha256": "1fd03b86d792f286b8134d7190d3a05277e35f93f34299ed11b71fd7216c61a7"},
 }
 
 
