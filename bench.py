@@ -408,7 +408,7 @@ def profile_case(spec: str, iters: int):
     spec: "attn:B,H,N[,causal][,d64]" | "attnnorm:B,H,N[,causal][,d64]" (the normalised
           form) | "attnqk:B,H,N[,causal]" (QK-norm inputs with
           their score bound) | "bwd:B,H,N[,causal][,d64]" | "softmax:rows,cols"
-          | "topk:rows,cols,k"
+          | "topk:rows,cols,k[,nospike]"
           | "decode:B,H,Nk[,splits]"
           | "append:B,H,Nk,n_new[,splits]" | "lsemerge:S,rows,d".
     Inputs come from the same generators as the full workloads.
@@ -468,7 +468,8 @@ def profile_case(spec: str, iters: int):
         work, unit = 8 * R * C, "GB/s"
     elif op == "topk":
         R, C, kk = (int(x) for x in parts[:3])
-        x = W.softmax_logits(2, rows=R, cols=C).to(dev)
+        spikes = 0.0 if "nospike" in parts[3:] else 0.01  # the workload's 1 % of entries at 40.0
+        x = W.softmax_logits(2, rows=R, cols=C, spike_frac=spikes).to(dev)
         ii = torch.empty((R, kk), dtype=torch.int32, device=dev)
         pp = torch.empty((R, kk), dtype=torch.float32, device=dev)
         run = lambda: osm.softmax_topk(x, kk, idx=ii, prob=pp)
