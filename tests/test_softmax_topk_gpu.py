@@ -116,6 +116,16 @@ def test_group_filter_edge_rows(cuda_ok):
         assert idx[3, 0] == cols - 1 and idx[3, 1] == cols - 2
 
 
+@pytest.mark.parametrize("k", [2, 8, 16, 32])
+def test_rows_without_ties(cuda_ok, k):
+    """2 N(0,1) entries with no repeated spike value: the group filter and the
+    candidate rounds on continuous data, rows of one CTA and of a cluster."""
+    for rows, cols in ((64, 32768), (3, 1 << 19)):
+        x = W.softmax_logits(seed=77 + k, rows=rows, cols=cols, spike_frac=0.0)
+        idx, prob = osm.softmax_topk(x.cuda(), k)
+        check(x, k, idx, prob)
+
+
 def test_full_size_rows(cuda_ok):
     """4096 x 32768 softmax workload (2 N(0,1), 1% of entries = 40.0), k = 8:
     every row's indices exactly, probabilities within the bar."""
